@@ -1,0 +1,134 @@
+"""Seeded synthetic inputs for the Ulysses low-precision quantize/pack path.
+
+Serves both the CUDA path and the CPU oracle; it holds none of the method's
+arithmetic (no amax, no scales of the path, no quantisation).  What it builds
+is what a caller hands the path:
+
+* Q, K, V on the global grid ``[B, S, H, D]`` as raw 16-bit patterns (bf16 or
+  fp16), and the per-rank shards ``[P, B, L, H, D]`` cut from them;
+* ``k_mean_global`` ``[B, H, D]``: the page "k_grouped_amax" (Parameters) says
+  the caller passes the global K mean rounded to the input dtype.  Here it is
+  the fp64 mean of the live rows ``[0, used)``, rounded to fp32, then to the
+  dtype;
+* ``v_scale`` ``[B, H, D]`` fp32: the page "unpack_for_sage" (Returns) leaves
+  the V scale with the caller.  Here it is the per-(batch, head, channel)
+  absolute maximum of V over the whole sequence (at least 1e-7) divided by
+  448, the largest finite E4M3 magnitude.
+
+Draw order (PCG64 ``default_rng(seed)``, float32 draws unless Student-t):
+Q; K channel means ``[H, D]`` (shared over the batch); K deviations
+``[B, S, H, D]``; V; then, when the workload has outliers, one uniform mask per
+tensor for Q, K, V in that order, multiplying the selected entries by the
+outlier factor.  Then the dtype cast (round to nearest even), the zero fill of
+padding rows ``[used, S)``, then ``k_mean_global`` and ``v_scale``.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+from .configs import BF16, FP16, Workload
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns, round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    return ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def f16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return b.view(np.float16).astype(np.float32)
+
+
+def to_bits(x: np.ndarray, dtype: int) -> np.ndarray:
+    return f32_to_bf16_bits(x) if dtype == BF16 else f32_to_f16_bits(x)
+
+
+def from_bits(b: np.ndarray, dtype: int) -> np.ndarray:
+    return bf16_bits_to_f32(b) if dtype == BF16 else f16_bits_to_f32(b)
+
+
+@dataclasses.dataclass
+class Inputs:
+    wl: Workload
+    q: np.ndarray          # uint16 [B, S, H, D]
+    k: np.ndarray          # uint16 [B, S, H, D]
+    v: np.ndarray          # uint16 [B, S, H, D]
+    k_mean: np.ndarray     # uint16 [B, H, D]
+    v_scale: np.ndarray    # float32 [B, H, D]
+
+    @property
+    def used(self) -> int:
+        u = self.wl.used_sequence
+        return self.wl.S if u is None else u
+
+    def shards(self, name: str) -> np.ndarray:
+        """Per-rank shards [P, B, L, H, D] (contiguous) of q, k or v."""
+        return shard(getattr(self, name), self.wl.P)
+
+
+def shard(x: np.ndarray, P: int) -> np.ndarray:
+    B, S, H, D = x.shape
+    L = S // P
+    return np.ascontiguousarray(x.reshape(B, P, L, H, D).transpose(1, 0, 2, 3, 4))
+
+
+def _draw(rng: np.random.Generator, dist: str, shape) -> np.ndarray:
+    if dist == "normal":
+        return rng.standard_normal(shape, dtype=np.float32)
+    if dist == "t3":
+        return rng.standard_t(3.0, shape).astype(np.float32)
+    raise ValueError(dist)
+
+
+def make_inputs(wl: Workload) -> Inputs:
+    rng = np.random.default_rng(wl.seed)
+    B, S, H, D = wl.B, wl.S, wl.H, wl.D
+    shape = (B, S, H, D)
+
+    q = _draw(rng, wl.qv_dist, shape)
+    mu = rng.standard_normal((H, D), dtype=np.float32) * np.float32(wl.k_mean_std)
+    kn = _draw(rng, wl.k_noise_dist, shape)
+    kn *= np.float32(wl.k_noise_std)
+    k = kn
+    k += mu[None, None, :, :]
+    del kn
+    v = _draw(rng, wl.qv_dist, shape)
+    if wl.outlier_frac > 0.0:
+        for x in (q, k, v):
+            m = rng.random(shape, dtype=np.float32) < np.float32(wl.outlier_frac)
+            x[m] *= np.float32(wl.outlier_mult)
+            del m
+
+    qb = to_bits(q, wl.dtype); del q
+    kb = to_bits(k, wl.dtype); del k
+    vb = to_bits(v, wl.dtype); del v
+
+    used = S if wl.used_sequence is None else wl.used_sequence
+    if used < S:
+        qb[:, used:] = 0
+        kb[:, used:] = 0
+        vb[:, used:] = 0
+
+    kf = from_bits(kb[:, :used], wl.dtype)
+    kmean64 = kf.mean(axis=1, dtype=np.float64)           # [B, H, D]
+    del kf
+    k_mean = to_bits(kmean64.astype(np.float32), wl.dtype)
+
+    vabs = np.abs(from_bits(vb, wl.dtype)).max(axis=1)     # [B, H, D] float32
+    v_scale = np.maximum(vabs, np.float32(1e-7)) / np.float32(448.0)
+    v_scale = v_scale.astype(np.float32)
+
+    return Inputs(wl=wl, q=qb, k=kb, v=vb, k_mean=np.ascontiguousarray(k_mean),
+                  v_scale=np.ascontiguousarray(v_scale))
