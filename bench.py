@@ -1,0 +1,361 @@
+"""Throughput of the Ulysses low-precision quantize -> pack -> unpack path.
+
+A step is one pass of the whole path (boundary min/max, derive, fused
+amax+pack with the exchange folded into its stores, unpack) over every rank of
+an emulated Ulysses group held on one GPU, on seeded synthetic inputs shaped
+like the long non-aligned workload (B=1, H=40, D=128, P=8, L=9360, bf16,
+used 74800).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun, one process per GPU) every GPU runs its own replica of
+the emulated group (no collective on the data path), so per-GPU work is fixed
+(weak scaling); value = bytes of all ranks / the slowest rank's time.
+``--impl reference`` times the CPU oracle instead, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective HBM GB/s (amax+pack+unpack) & % of GB300 HBM peak; tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None, help="workload name (default: the headline one)")
+    ap.add_argument("--mode", choices=["fused", "unfused"], default="fused")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="minimum CPU time spent on the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons) with host
+    timestamps; only samples inside [t0, t1] of the timed region are kept."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str | None):
+        self.samples = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        if gpu_index is not None:
+            cmd += ["-i", gpu_index]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.monotonic(), line.strip()))
+
+    def wait_first(self, timeout=5.0):
+        t = time.monotonic()
+        while self.proc and not self.samples and time.monotonic() - t < timeout:
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.samples:
+            if t0 - 0.06 <= ts <= t1 + 0.06:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) == 8:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in timed region"],
+                    "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows),
+                "power_w_max": max((float(r[2]) for r in rows
+                                    if r[2].replace(".", "").isdigit()), default=None)}
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_sample(wl):
+    """A bounded sample of one step for the CPU oracle: rank 0's sender work
+    (k_grouped_amax, boundary min/max of every rank, derive, pack) and
+    destination 0's receiver work (unpack_for_sage), on the workload with one
+    head per destination (H = P; L, P, D, dtype and padding unchanged).  The
+    receiver is fed rank 0's chunk in every source slot (the oracle's loops do
+    the same work whatever the bytes).  Returns (callable, algorithmic bytes)."""
+    import numpy as np
+
+    from oracle import oracle as O
+    from quantize_pack_gb300 import metrics, synth
+
+    swl = wl.replace(H=wl.P, name=wl.name + "_h1")
+    inp = synth.make_inputs(swl)
+    q, k, v = inp.shards("q"), inp.shards("k"), inp.shards("v")
+    P, L = swl.P, swl.L
+
+    def run():
+        a = O.k_grouped_amax(k[0], inp.k_mean, swl.dtype, rank=0, world_size=P,
+                             used_sequence=swl.used_sequence)
+        mm, qb = zip(*[O.boundary_minmax(k[r], q[r], swl.dtype, rank=r, world_size=P,
+                                         used_sequence=swl.used_sequence) for r in range(P)])
+        g = np.ascontiguousarray(np.stack(mm))
+        gq = np.ascontiguousarray(np.stack(qb))
+        O.derive_k_boundary_amax(a, g, inp.k_mean, swl.dtype, rank=0, local_sequence=L,
+                                 world_size=P)
+        send = O.pack(q[0], k[0], v[0], inp.k_mean, swl.dtype, a, gq, inp.v_scale, rank=0,
+                      world_size=P)
+        recv0 = np.ascontiguousarray(np.broadcast_to(send[0], send.shape))
+        O.unpack_for_sage(recv0, batch_size=swl.B, local_sequence=L, local_heads=1,
+                          head_dim=swl.D, world_size=P, scale_sequence=swl.scale_sequence)
+
+    return run, metrics.step_bytes(swl) / P, swl
+
+
+def run_reference(args, wl, rank):
+    if rank != 0:
+        return
+    run, nbytes, swl = oracle_sample(wl)
+    for _ in range(args.warmup):
+        run()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t) / args.steps
+    value = nbytes / dt / 1e9
+    sample = (f"per step: rank 0 sender + destination 0 receiver of {swl.name} "
+              f"(H={swl.H}, one head per destination), {nbytes / 1e6:.1f} MB algorithmic")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, **{k: v for k, v in wl.describe().items() if k != "workload"}},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args, wl, rank, world, dist):
+    import numpy as np
+    import torch
+
+    from quantize_pack_gb300 import metrics, synth, ulp
+    from quantize_pack_gb300.path import UlyssesLowpPath
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ulp.lib()                                               # fail loudly if not built
+    dt = torch.bfloat16 if wl.dtype == 0 else torch.float16
+
+    inp = synth.make_inputs(wl)
+    host = {n: torch.from_numpy(np.ascontiguousarray(inp.shards(n)).view(np.int16)).view(dt)
+            for n in "qkv"}
+    km_h = torch.from_numpy(inp.k_mean.view(np.int16)).view(dt)
+    vs_h = torch.from_numpy(inp.v_scale)
+    q, k, v = (host[n].to(dev) for n in "qkv")
+    km, vs = km_h.to(dev), vs_h.to(dev)
+    path = UlyssesLowpPath(B=wl.B, L=wl.L, H=wl.H, D=wl.D, world_size=wl.P, dtype=dt,
+                           used_sequence=wl.used_sequence, scale_sequence=wl.scale_sequence,
+                           aligned=wl.aligned, fused=(args.mode == "fused"), fold_exchange=True,
+                           device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        path.run(q, k, v, km, vs)
+    torch.cuda.synchronize()
+
+    gpu_id = None
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        u = str(getattr(props, "uuid", ""))
+        if u:
+            gpu_id = u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        gpu_id = None
+    sampler = ClockSampler(gpu_id)
+    sampler.wait_first()
+
+    K = args.steps
+    ev_pack = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    start.record(stream)
+    for i in range(K):
+        e0, e1 = ev_pack[i]
+        path.run(q, k, v, km, vs, on_pack=(lambda e=e0: e.record(stream), lambda e=e1: e.record(stream)))
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    barrier()
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+
+    ms = start.elapsed_time(end) / K
+    pack_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev_pack)
+    if dist is not None:
+        t = torch.tensor([ms, pack_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, pack_ms = float(t[0]), float(t[1])
+
+    # ---- end to end through the public API with host buffers
+    E = max(1, args.e2e_steps)
+    pin = {n: host[n].pin_memory() for n in "qkv"}
+    km_p, vs_p = km_h.pin_memory(), vs_h.pin_memory()
+    outs_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in path.out]
+
+    def e2e_step():
+        q.copy_(pin["q"], non_blocking=True)
+        k.copy_(pin["k"], non_blocking=True)
+        v.copy_(pin["v"], non_blocking=True)
+        km.copy_(km_p, non_blocking=True)
+        vs.copy_(vs_p, non_blocking=True)
+        outs = path.run(q, k, v, km, vs)
+        for h_, d_ in zip(outs_h, outs):
+            h_.copy_(d_, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for _ in range(E):
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = es.elapsed_time(ee) / E
+    if dist is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    h2d = sum(t.numel() * t.element_size() for t in (pin["q"], pin["k"], pin["v"], km_p, vs_p))
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+
+    if rank != 0:
+        return
+    step_bytes = metrics.step_bytes(wl)
+    value = step_bytes * world / (ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    pack_gbs = metrics.pack_bytes(wl) / (pack_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": wl.name, **{k_: v_ for k_, v_ in wl.describe().items() if k_ != "workload"},
+            "path": f"{args.mode} amax+pack (exchange folded into the stores) + unpack, "
+                    f"{path.launches_per_step} launches/step",
+            "l2": f"inputs {6 * wl.N / 1e9:.2f} GB > 129 MB L2; no flush",
+            "parallelism": f"{world} independent replica(s) of a P={wl.P} emulated Ulysses group",
+        },
+        "tokens_per_s": wl.tokens * world / (ms * 1e-3),
+        "hbm_frac": value / world / peak,
+        "step_bytes": step_bytes,
+        "roofline": {"bound": "hbm", "kernel": "pack_kernel", "achieved": pack_gbs, "peak": peak,
+                     "peak_kind": f"{peak_kind} (STREAM copy)", "unit": "GB/s",
+                     "frac": pack_gbs / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": metrics.pack_bytes(wl),
+                     "launch_ms": pack_ms},
+        "e2e": {"value": step_bytes * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "steps": E, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * path.launches_per_step,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        run, nbytes, swl = oracle_sample(wl)
+        n, t = 0, time.perf_counter()
+        while True:
+            run()
+            n += 1
+            if time.perf_counter() - t >= args.cpu_seconds:
+                break
+        dtc = (time.perf_counter() - t) / n
+        line["cpu_baseline"] = {
+            "value": nbytes / dtc / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} x (rank 0 sender + destination 0 receiver of {swl.name}, "
+                      f"{nbytes / 1e6:.1f} MB algorithmic each)"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    from quantize_pack_gb300 import configs
+    wl = configs.BY_NAME[args.workload] if args.workload else configs.HEADLINE
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        run_reference(args, wl, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist_
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist_.init_process_group(backend)
+        dist = dist_
+    try:
+        run_ours(args, wl, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

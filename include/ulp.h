@@ -1,0 +1,207 @@
+/*
+ * ulp.h -- C ABI of the GB300 (sm_103a) Ulysses low-precision quantize/pack path.
+ *
+ * The path feeds an INT8-QK / FP8-PV ("Sage") attention kernel after a Ulysses
+ * all-to-all.  Per rank r of a Ulysses group of P ranks, rank r holds global
+ * sequence rows [r*L, (r+1)*L) of Q, K, V [B, L, H, D]; after the exchange a
+ * destination holds all S = P*L rows of h = H/P heads.  The entry points are:
+ *
+ *   ulp_k_grouped_amax          page "flashinfer.comm._ulysses_lowp.k_grouped_amax"
+ *   ulp_boundary_minmax         page "...derive_k_boundary_amax" (gathered_minmax parameter:
+ *                               the raw-K boundary min/max every rank contributes)
+ *   ulp_derive_k_boundary_amax  page "...derive_k_boundary_amax"
+ *   ulp_pack                    the sender pack (INT8 Q/K, FP8 E4M3 V into source-major
+ *                               chunks); page "...unpack_for_sage" (recv_u8 parameter,
+ *                               Returns: the V scale stays with the caller)
+ *   ulp_alltoall_emulate        the all-to-all of the chunks, as a device-local copy
+ *   ulp_unpack_for_sage         page "...unpack_for_sage"
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer the caller owns; the library
+ *    allocates nothing and keeps no state across calls except a thread-local
+ *    last-error string.  Tensors are dense, row-major (C order).  Q, K, V,
+ *    k_mean, v_scale, the chunk buffers and q8/k8/v8 must be 16-byte aligned;
+ *    the other fp32 buffers (amax, min/max, partials, scales) 4-byte aligned.
+ *  - `dtype` is ULP_BF16 or ULP_FP16 for Q/K/V/k_mean.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and runs asynchronously; a call returns once its launches are
+ *    enqueued.
+ *  - Return value: ULP_OK (0) or a negative status.  Arguments are validated
+ *    before any launch, so a call that returns ULP_EINVAL / ULP_EDTYPE /
+ *    ULP_EALIGN has enqueued nothing and left every output untouched.
+ *    ULP_ECUDA reports a launch failure (cudaGetLastError after the launch).
+ *    ulp_last_error() returns a message for the calling thread's last failure.
+ *  - Optional integers use -1 for "None": used_sequence, scale_sequence,
+ *    aligned (-1 None, 0 False, 1 True), enable_pdl (-1 select by device
+ *    support, 0 off, 1 on; accepted and validated, launches are plain).
+ *  - world_size is 2, 4, 6 or 8 (6: structurally supported, not validated by
+ *    the method's authors); head_dim D is 64 or 128; H % world_size == 0.
+ *  - rank is in [0, world_size), or ULP_ALL_RANKS: one launch covers every
+ *    rank of an emulated Ulysses group held on one GPU.  Then each per-rank
+ *    tensor is the stack of all ranks' tensors along a new leading axis of
+ *    size world_size (written [P, ...] below).
+ *
+ * Geometry (K groups of 64 rows, Q groups of 128 rows, both on the global row
+ * grid): first_G(r) = (r*L)/G, last_G(r) = ((r+1)*L-1)/G; slot j of rank r is
+ * global group first_G(r)+j; slots(L, G) = ceil(L/G) + (L % G != 0) bounds
+ * the groups any rank touches.  Slots past the groups a rank touches hold
+ * the floor value 1e-7 (amax) / rn(1e-7/127) (scale).
+ *
+ * Chunk layout (one source rank -> one destination), each section 16-byte
+ * aligned, in this order:
+ *   Q int8 [B, L, h, D] | K int8 [B, L, h, D] | V e4m3 [B, L, h, D] |
+ *   q_scale f32 [B, h, slots(L,128)] | k_scale f32 [B, h, slots(L,64)]
+ * Chunk p of a source carries global heads [p*h, (p+1)*h).
+ */
+#ifndef ULP_H
+#define ULP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void *ulp_stream_t; /* a cudaStream_t */
+
+enum { ULP_BF16 = 0, ULP_FP16 = 1 };
+
+enum {
+    ULP_OK = 0,
+    ULP_EINVAL = -1, /* argument outside its domain, inconsistent shapes, size overflow */
+    ULP_EDTYPE = -2, /* dtype is neither ULP_BF16 nor ULP_FP16 */
+    ULP_EALIGN = -3, /* a pointer is NULL or misaligned */
+    ULP_ECUDA = -4   /* a CUDA launch or copy failed */
+};
+
+enum {
+    ULP_SEND_SOURCE_MAJOR = 0, /* send[src][dst][chunk]: each rank's own send buffer */
+    ULP_SEND_DEST_MAJOR = 1    /* send[dst][src][chunk]: the receivers' recv_u8 buffers */
+};
+
+#define ULP_ALL_RANKS (-1)
+
+/* slots(L, G): per-rank slot count for groups of G rows (G = 64 for K, 128 for
+ * Q): ceil(L/G) + (L % G != 0).  Page "k_grouped_amax" (Returns:
+ * [B, H, slots(L, 64)]) names it without printing it; this is the plainest
+ * bound in (L, G) alone.  Returns -1 (ULP_EINVAL) for L < 1 or G < 1. */
+int ulp_slots(int local_sequence, int group);
+
+/* scale_widths(n) of page "unpack_for_sage" (scale_sequence paragraph):
+ * consumer scale widths for n rows, *q_width = ceil(n/128),
+ * *k_width = ceil(n/64).  ULP_EINVAL for n < 1 or NULL outputs. */
+int ulp_scale_widths(int n, int *q_width, int *k_width);
+
+/* Bytes of one chunk (layout above) for batch B, shard length L, h heads per
+ * destination, head dim D.  ULP_EINVAL for non-positive sizes. */
+int ulp_chunk_bytes(int B, int L, int h, int D, size_t *chunk_bytes);
+
+/* Byte offsets of the five chunk sections: offsets[0..4] = Q, K, V,
+ * q_scale, k_scale. */
+int ulp_chunk_offsets(int B, int L, int h, int D, size_t offsets[5]);
+
+/* k_grouped_amax -- page "flashinfer.comm._ulysses_lowp.k_grouped_amax".
+ * For each (b, head, slot j) of rank r:
+ *   out[b,H,j] = max(1e-7, max |rn(f32(k[b,t,H,d]) - f32(k_mean[b,H,d]))|)
+ * over the rank's rows t of global K group first_64(r)+j and all d.  With
+ * used_sequence < S, the slot of the partial live group (used-1)/64 is taken
+ * over live rows t < used only; all other slots (fully padded groups
+ * included) keep the value over all their rows.  used_sequence = -1 or S
+ * changes nothing.  Rows >= used must be zero-filled by the caller.
+ *   k       [B, L, H, D] dtype     ([P, B, L, H, D] for ULP_ALL_RANKS)
+ *   k_mean  [B, H, D] dtype: the global K mean rounded to dtype
+ *   out     [B, H, slots(L,64)] fp32 ([P, B, H, slots] for ULP_ALL_RANKS) */
+int ulp_k_grouped_amax(const void *k, const void *k_mean, int dtype, int B, int L, int H, int D,
+                       int rank, int world_size, int used_sequence, float *out, int enable_pdl,
+                       ulp_stream_t stream);
+
+/* Raw-K boundary min/max of a rank -- the payload the page
+ * "derive_k_boundary_amax" gathers ("AllGather #1 under stats protocol 2"):
+ *   minmax[b,H,e,0,d] = min, minmax[b,H,e,1,d] = max of f32(k[b,t,H,d]) over
+ *   the rank's live rows t < used of its first (e = 0) / last (e = 1) touched
+ *   K group; +inf / -inf when that slice has no live row; -0 stored as +0; a
+ *   rank touching one group writes it under both e.
+ * Also the Q boundary partials (input of ulp_pack):
+ *   q_partial[b,H,e] = max(1e-7, max |f32(q[b,t,H,d])|) over the rank's rows
+ *   of its first (e = 0) / last (e = 1) touched 128-row Q group.
+ *   k, q       [B, L, H, D] dtype  ([P, ...] for ULP_ALL_RANKS)
+ *   minmax     [B, H, 2, 2, D] fp32 ([P, B, H, 2, 2, D] = the gathered buffer
+ *              in group-rank order, for ULP_ALL_RANKS)
+ *   q_partial  [B, H, 2] fp32 ([P, B, H, 2] for ULP_ALL_RANKS) */
+int ulp_boundary_minmax(const void *k, const void *q, int dtype, int B, int L, int H, int D,
+                        int rank, int world_size, int used_sequence, float *minmax,
+                        float *q_partial, ulp_stream_t stream);
+
+/* derive_k_boundary_amax -- page "flashinfer.comm._ulysses_lowp.derive_k_boundary_amax".
+ * Overwrites, in place, rank r's boundary slots (its first and last touched K
+ * group g) with max over every rank r' touching g of
+ *   max(1e-7, max_d max(rn(maxK[r',g,d] - m[d]), rn(m[d] - minK[r',g,d])))
+ * which equals the amax over the whole group (monotone rn subtraction).  Other
+ * slots are left as they are.
+ *   grouped_amax    [B, H, slots(L,64)] fp32, in place ([P, ...] for ULP_ALL_RANKS)
+ *   gathered_minmax [P, B, H, 2, 2, D] fp32 (from ulp_boundary_minmax)
+ *   k_mean          [B, H, D] dtype */
+int ulp_derive_k_boundary_amax(float *grouped_amax, const float *gathered_minmax,
+                               const void *k_mean, int dtype, int B, int H, int D, int rank,
+                               int local_sequence, int world_size, ulp_stream_t stream);
+
+/* Sender pack of rank r into its P chunks (layout above).
+ *   Q amax of 128-row group g: max(1e-7, max |f32(q)|) over g's rows; for the
+ *   rank's first/last touched Q group it is the max of gathered_q_partial over
+ *   the ranks touching g, otherwise computed from the rank's own rows.
+ *   K amax: k_amax slots.  fused = 0: every slot is read from k_amax (the
+ *   output of ulp_k_grouped_amax after ulp_derive_k_boundary_amax).  fused = 1:
+ *   only the boundary slots (first/last touched) are read -- they must hold
+ *   the derived values -- and the other slots are computed from the rank's own
+ *   K rows in the same pass and written to k_amax (same values as fused = 0).
+ *   scale = rn(amax / 127); q8 = sat8(rne(rn(f32(q) / qs))),
+ *   k8 = sat8(rne(rn(rn(f32(k) - f32(m)) / ks))),
+ *   v8 = e4m3_satfinite_rn(rn(f32(v) / v_scale[b,H,d])).
+ *   q, k, v             [B, L, H, D] dtype ([P, ...] for ULP_ALL_RANKS)
+ *   k_mean              [B, H, D] dtype
+ *   k_amax              [B, H, slots(L,64)] fp32 ([P, ...] for ULP_ALL_RANKS)
+ *   gathered_q_partial  [P, B, H, 2] fp32 (from ulp_boundary_minmax)
+ *   v_scale             [B, H, D] fp32, the caller's V scale (per global head)
+ *   send                ULP_SEND_SOURCE_MAJOR: [P, chunk_bytes] of this rank
+ *                       ([P_src, P_dst, chunk_bytes] for ULP_ALL_RANKS);
+ *                       ULP_SEND_DEST_MAJOR: [P_dst, P_src, chunk_bytes], the
+ *                       receive buffers of every destination: chunk (r, p) is
+ *                       written at [p][r] (the exchange folded into the stores). */
+int ulp_pack(const void *q, const void *k, const void *v, const void *k_mean, int dtype,
+             float *k_amax, const float *gathered_q_partial, const float *v_scale, int B, int L,
+             int H, int D, int rank, int world_size, int used_sequence, int fused, uint8_t *send,
+             int send_layout, int enable_pdl, ulp_stream_t stream);
+
+/* The all-to-all, emulated on one GPU: recv[p][s] = send[s][p] for the
+ * [P, P, chunk_bytes] buffers of all ranks (page "unpack_for_sage": recv_u8 is
+ * the source-major buffer received by all-to-all). */
+int ulp_alltoall_emulate(const uint8_t *send, uint8_t *recv, int world_size, size_t chunk_bytes,
+                         ulp_stream_t stream);
+
+/* unpack_for_sage -- page "flashinfer.comm._ulysses_lowp.unpack_for_sage".
+ * From recv_u8 [P, chunk_bytes] of one destination:
+ *   q8, k8 [B, S, h, D] int8:   q8[b, s*L+t, j, d] = chunk_s.Q[b, t, j, d]
+ *   v8 [B, D, h, Spad] e4m3, Spad = ceil(S/64)*64:
+ *        v8[b, d, j, t] = chunk_{t/L}.V[b, t%L, j, d] for t < S, 0 for t >= S
+ *   q_scale [B, h, Wq], k_scale [B, h, Wk] fp32, (Wq, Wk) = scale_widths(n),
+ *        n = scale_sequence (S when -1); slot g is taken from the source that
+ *        holds the group's first row.
+ * aligned = 1 requires L % 128 == 0 (ULP_EINVAL otherwise); the values never
+ * depend on it.  num_dests >= 1 destinations are unpacked in one launch:
+ * recv is [num_dests, P, chunk_bytes] and every output gains a leading
+ * num_dests axis (num_dests = 1 is the single-destination call). */
+int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int D, int world_size,
+                        int aligned, int scale_sequence, int8_t *q8, int8_t *k8, uint8_t *v8,
+                        float *q_scale, float *k_scale, int num_dests, int enable_pdl,
+                        ulp_stream_t stream);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char *ulp_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ULP_H */

@@ -1,0 +1,129 @@
+// Host side of the ulp library: status reporting, argument checks, geometry
+// queries and the emulated all-to-all.
+#include <cstring>
+#include <string>
+
+#include "ulp_internal.cuh"
+
+namespace ulp {
+
+static thread_local std::string g_last_error;
+
+int fail(int status, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return status;
+}
+
+int check_launch(const char *what)
+{
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(ULP_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ULP_OK;
+}
+
+bool aligned16(const void *p) { return p != nullptr && ((uintptr_t)p & 15u) == 0; }
+bool aligned4(const void *p) { return p != nullptr && ((uintptr_t)p & 3u) == 0; }
+
+int check_world(int world_size)
+{
+    if (world_size != 2 && world_size != 4 && world_size != 6 && world_size != 8)
+        return fail(ULP_EINVAL, "world_size must be 2, 4, 6 or 8 (got %d)", world_size);
+    return ULP_OK;
+}
+
+int check_common(int dtype, int B, int L, int H, int D, int rank, int world_size,
+                 int used_sequence, int enable_pdl)
+{
+    if (dtype != ULP_BF16 && dtype != ULP_FP16)
+        return fail(ULP_EDTYPE, "dtype must be ULP_BF16 or ULP_FP16 (got %d)", dtype);
+    if (int s = check_world(world_size)) return s;
+    if (B < 1 || L < 1 || H < 1) return fail(ULP_EINVAL, "B, L, H must be positive (%d, %d, %d)", B, L, H);
+    if (D != 64 && D != 128) return fail(ULP_EINVAL, "head_dim must be 64 or 128 (got %d)", D);
+    if (H % world_size != 0)
+        return fail(ULP_EINVAL, "H (%d) must be a multiple of world_size (%d)", H, world_size);
+    if (rank != ULP_ALL_RANKS && (rank < 0 || rank >= world_size))
+        return fail(ULP_EINVAL, "rank %d outside [0, %d)", rank, world_size);
+    if ((long long)L * world_size > INT_MAX / 2)
+        return fail(ULP_EINVAL, "sequence length %lld too large", (long long)L * world_size);
+    const int S = L * world_size;
+    if (used_sequence != -1 && (used_sequence < 1 || used_sequence > S))
+        return fail(ULP_EINVAL, "used_sequence %d outside [1, %d]", used_sequence, S);
+    if (enable_pdl < -1 || enable_pdl > 1)
+        return fail(ULP_EINVAL, "enable_pdl must be -1, 0 or 1 (got %d)", enable_pdl);
+    // every per-rank tensor must stay addressable with 64-bit offsets and every
+    // grid within int range
+    if ((double)B * S * H * D > 4.0e15) return fail(ULP_EINVAL, "tensor too large");
+    return ULP_OK;
+}
+
+}  // namespace ulp
+
+using namespace ulp;
+
+extern "C" {
+
+const char *ulp_last_error(void) { return g_last_error.c_str(); }
+
+int ulp_slots(int local_sequence, int group)
+{
+    if (local_sequence < 1 || group < 1)
+        return fail(ULP_EINVAL, "slots: L and group must be positive (%d, %d)", local_sequence, group);
+    return slots(local_sequence, group);
+}
+
+int ulp_scale_widths(int n, int *q_width, int *k_width)
+{
+    if (n < 1 || !q_width || !k_width) return fail(ULP_EINVAL, "scale_widths: n must be positive (%d)", n);
+    *q_width = (n + kGQ - 1) / kGQ;
+    *k_width = (n + kGK - 1) / kGK;
+    return ULP_OK;
+}
+
+int ulp_chunk_offsets(int B, int L, int h, int D, size_t offsets[5])
+{
+    if (B < 1 || L < 1 || h < 1 || D < 1 || !offsets)
+        return fail(ULP_EINVAL, "chunk_offsets: sizes must be positive");
+    ChunkLayout c = chunk_layout(B, L, h, D);
+    offsets[0] = c.q;
+    offsets[1] = c.k;
+    offsets[2] = c.v;
+    offsets[3] = c.qs;
+    offsets[4] = c.ks;
+    return ULP_OK;
+}
+
+int ulp_chunk_bytes(int B, int L, int h, int D, size_t *chunk_bytes)
+{
+    if (B < 1 || L < 1 || h < 1 || D < 1 || !chunk_bytes)
+        return fail(ULP_EINVAL, "chunk_bytes: sizes must be positive");
+    *chunk_bytes = chunk_layout(B, L, h, D).bytes;
+    return ULP_OK;
+}
+
+int ulp_alltoall_emulate(const uint8_t *send, uint8_t *recv, int world_size, size_t chunk_bytes,
+                         ulp_stream_t stream)
+{
+    if (int s = check_world(world_size)) return s;
+    if (chunk_bytes == 0 || chunk_bytes % 16 != 0)
+        return fail(ULP_EINVAL, "chunk_bytes must be a positive multiple of 16");
+    if (!aligned16(send) || !aligned16(recv)) return fail(ULP_EALIGN, "send/recv must be 16-byte aligned");
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t P = (size_t)world_size;
+    // recv[p][s] = send[s][p]: for each source s, a 2-D copy of P chunks
+    // (source pitch chunk_bytes, destination pitch P*chunk_bytes).
+    for (size_t s = 0; s < P; ++s) {
+        cudaError_t e = cudaMemcpy2DAsync(recv + s * chunk_bytes, P * chunk_bytes,
+                                          send + s * P * chunk_bytes, chunk_bytes, chunk_bytes, P,
+                                          cudaMemcpyDeviceToDevice, st);
+        if (e != cudaSuccess) return fail(ULP_ECUDA, "alltoall copy: %s", cudaGetErrorString(e));
+    }
+    return ULP_OK;
+}
+
+}  // extern "C"

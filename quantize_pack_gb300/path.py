@@ -1,0 +1,92 @@
+"""The whole quantize -> pack -> exchange -> unpack path of an emulated Ulysses
+group of P ranks held on one GPU.
+
+All P shards sit in device memory; the stats all-gather is the stacked
+[P, ...] buffer the boundary kernel writes, and the all-to-all is folded into
+the pack's store addresses (dest-major send buffer = every destination's
+recv_u8) or, on request, run as a separate device copy.  One step is four
+launches of the CUDA library: boundary min/max -> derive -> pack -> unpack
+(plus k_grouped_amax when the unfused pack is chosen, plus the copy when the
+exchange is not folded).
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import ulp
+
+
+class UlyssesLowpPath:
+    def __init__(self, *, B: int, L: int, H: int, D: int, world_size: int, dtype: torch.dtype,
+                 used_sequence: Optional[int] = None, scale_sequence: Optional[int] = None,
+                 aligned: Optional[bool] = None, fused: bool = True, fold_exchange: bool = True,
+                 device="cuda"):
+        P = world_size
+        self.B, self.L, self.H, self.D, self.P = B, L, H, D, P
+        self.h = H // P
+        self.S = P * L
+        self.dtype = dtype
+        self.used_sequence = used_sequence
+        self.scale_sequence = scale_sequence
+        self.aligned = aligned
+        self.fused = fused
+        self.fold_exchange = fold_exchange
+        self.device = torch.device(device)
+        self.chunk_bytes = ulp.chunk_bytes(B, L, self.h, D)
+        f32 = dict(dtype=torch.float32, device=self.device)
+        self.k_amax = torch.empty((P, B, H, ulp.slots(L, ulp.GK)), **f32)
+        self.minmax = torch.empty((P, B, H, 2, 2, D), **f32)
+        self.q_partial = torch.empty((P, B, H, 2), **f32)
+        u8 = dict(dtype=torch.uint8, device=self.device)
+        self.recv = torch.empty((P, P, self.chunk_bytes), **u8)
+        self.send = None if fold_exchange else torch.empty((P, P, self.chunk_bytes), **u8)
+        self.out = ulp.unpack_outputs(B, L, self.h, D, P, scale_sequence, self.device, num_dests=P)
+
+    @property
+    def launches_per_step(self) -> int:
+        return 4 + (0 if self.fused else 1)
+
+    @property
+    def copies_per_step(self) -> int:
+        return 0 if self.fold_exchange else P_copies(self.P)
+
+    def run(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, k_mean: torch.Tensor,
+            v_scale: torch.Tensor, on_pack=None):
+        """q, k, v: stacked shards [P, B, L, H, D]; k_mean [B, H, D] (input
+        dtype); v_scale [B, H, D] fp32.  Returns the per-destination outputs
+        (q8, k8, v8, q_scale, k_scale), each with a leading P axis.
+        ``on_pack`` (optional) is a pair of callables run right before and
+        after the pack launch (used to time it)."""
+        P, L = self.P, self.L
+        if not self.fused:
+            ulp.k_grouped_amax(k, k_mean, rank=None, world_size=P,
+                               used_sequence=self.used_sequence, out=self.k_amax)
+        ulp.boundary_minmax(k, q, rank=None, world_size=P, used_sequence=self.used_sequence,
+                            out=(self.minmax, self.q_partial))
+        ulp.derive_k_boundary_amax(self.k_amax, self.minmax, k_mean, rank=None, local_sequence=L,
+                                   world_size=P)
+        if on_pack is not None:
+            on_pack[0]()
+        if self.fold_exchange:
+            ulp.pack(q, k, v, k_mean, self.k_amax, self.q_partial, v_scale, rank=None,
+                     world_size=P, used_sequence=self.used_sequence, fused=self.fused,
+                     send=self.recv, send_layout=ulp.SEND_DEST_MAJOR)
+        else:
+            ulp.pack(q, k, v, k_mean, self.k_amax, self.q_partial, v_scale, rank=None,
+                     world_size=P, used_sequence=self.used_sequence, fused=self.fused,
+                     send=self.send, send_layout=ulp.SEND_SOURCE_MAJOR)
+        if on_pack is not None:
+            on_pack[1]()
+        if not self.fold_exchange:
+            ulp.alltoall_emulate(self.send, self.recv)
+        return ulp.unpack_for_sage(self.recv, batch_size=self.B, local_sequence=L,
+                                   local_heads=self.h, head_dim=self.D, world_size=P,
+                                   aligned=self.aligned, scale_sequence=self.scale_sequence,
+                                   out=self.out)
+
+
+def P_copies(P: int) -> int:
+    """Copies the emulated all-to-all issues (one 2-D copy per source)."""
+    return P

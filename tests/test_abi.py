@@ -1,0 +1,98 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, its host geometry agrees with the oracle's (two independent
+implementations), and argument checks reject bad calls before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import oracle as O
+from quantize_pack_gb300 import build as B
+from quantize_pack_gb300 import ulp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build_library()
+    return ulp.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "ulp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ulp_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_geometry_agrees_with_oracle(lib):
+    for L in list(range(1, 400)) + [1000, 4096, 9360, 16384]:
+        for G in (64, 128):
+            assert ulp.slots(L, G) == O.slots(L, G)
+    for n in range(1, 1200):
+        assert ulp.scale_widths(n) == O.scale_widths(n)
+    for Bb, L, h, D in [(1, 96, 4, 64), (1, 1000, 4, 128), (2, 4096, 3, 128), (1, 9360, 5, 128),
+                        (4, 16384, 16, 64), (3, 17, 3, 64), (2, 1, 1, 128)]:
+        lay = O.chunk_layout(Bb, L, h, D)
+        assert ulp.chunk_bytes(Bb, L, h, D) == lay["chunk_bytes"]
+        assert ulp.chunk_offsets(Bb, L, h, D) == (lay["q"], lay["k"], lay["v"], lay["q_scale"],
+                                                 lay["k_scale"])
+
+
+FAKE = 1 << 20   # an aligned, never-dereferenced address: every call below fails validation
+
+
+@pytest.mark.parametrize("args,status", [
+    # dtype
+    (dict(dtype=7), -2),
+    # world size, rank, head dim, heads, used
+    (dict(world_size=3), -1), (dict(world_size=16), -1), (dict(rank=2, world_size=2), -1),
+    (dict(rank=-2), -1), (dict(D=96), -1), (dict(H=6, world_size=4), -1),
+    (dict(used=0), -1), (dict(used=2 * 96 + 1), -1), (dict(L=0), -1), (dict(B=0), -1),
+    (dict(pdl=2), -1),
+    # alignment
+    (dict(k=FAKE + 8), -3), (dict(k=0), -3), (dict(out=FAKE + 2), -3), (dict(km=FAKE + 4), -3),
+])
+def test_k_grouped_amax_rejects(lib, args, status):
+    a = dict(k=FAKE, km=FAKE, dtype=0, B=1, L=96, H=8, D=64, rank=0, world_size=2, used=-1,
+             out=FAKE, pdl=-1)
+    a.update(args)
+    got = lib.ulp_k_grouped_amax(a["k"], a["km"], a["dtype"], a["B"], a["L"], a["H"], a["D"],
+                                 a["rank"], a["world_size"], a["used"], a["out"], a["pdl"], None)
+    assert got == status
+    assert lib.ulp_last_error() != b""
+
+
+def test_unpack_rejects(lib):
+    ok = dict(recv=FAKE, B=1, L=96, h=4, D=64, P=2, aligned=-1, sseq=-1, q8=FAKE, k8=FAKE,
+              v8=FAKE, qs=FAKE, ks=FAKE, nd=1, pdl=-1)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.ulp_unpack_for_sage(a["recv"], a["B"], a["L"], a["h"], a["D"], a["P"],
+                                       a["aligned"], a["sseq"], a["q8"], a["k8"], a["v8"],
+                                       a["qs"], a["ks"], a["nd"], a["pdl"], None)
+    assert call(aligned=1) == -1                       # L % 128 != 0
+    assert b"aligned" in lib.ulp_last_error()
+    assert call(sseq=0) == -1 and call(sseq=193) == -1
+    assert call(P=5) == -1 and call(D=32) == -1 and call(nd=0) == -1
+    assert call(v8=FAKE + 1) == -3
+
+
+def test_pack_and_derive_reject(lib):
+    base = [FAKE] * 8
+    # fused must be 0/1, send_layout 0/1
+    assert lib.ulp_pack(*base[:4], 0, *base[4:7], 1, 96, 8, 64, 0, 2, -1, 2, FAKE, 0, -1, None) == -1
+    assert lib.ulp_pack(*base[:4], 0, *base[4:7], 1, 96, 8, 64, 0, 2, -1, 1, FAKE, 3, -1, None) == -1
+    assert lib.ulp_pack(*base[:4], 0, *base[4:7], 1, 96, 8, 64, 0, 2, -1, 1, FAKE + 2, 0, -1, None) == -3
+    assert lib.ulp_derive_k_boundary_amax(FAKE, FAKE, FAKE, 1, 1, 8, 64, 2, 96, 2, None) == -1
+    assert lib.ulp_boundary_minmax(FAKE, FAKE, 0, 1, 96, 8, 64, 0, 2, 500, FAKE, FAKE, None) == -1
+    assert lib.ulp_alltoall_emulate(FAKE, FAKE, 2, 24, None) == -1
