@@ -164,7 +164,8 @@ static size_t a16(size_t x) { return (x + 15) & ~(size_t)15; }
  *   Q int8 [B, L, h, D] | K int8 [B, L, h, D] | V e4m3 [B, L, h, D] |
  *   q_scale f32 [B, h, slots(L,128)] | k_scale f32 [B, h, slots(L,64)]
  * each section starting on a 16-byte boundary (a reading of this library:
- * the pages say only that recv_u8 is source-major [world_size, chunk_bytes]). */
+ * the pages say only that recv_u8 is source-major [world_size, chunk_bytes]).
+ * The alignment padding between sections is zero. */
 void orc_chunk_layout(int B, int L, int h, int D, size_t *off_q, size_t *off_k, size_t *off_v,
                       size_t *off_qs, size_t *off_ks, size_t *chunk_bytes)
 {
@@ -329,7 +330,8 @@ void orc_derive_k_boundary_amax(float *grouped_amax, const float *gathered, cons
  *  - chunk p (= global head H / h) receives heads [p*h, (p+1)*h), local head
  *    j = H % h, in the layout of orc_chunk_layout.
  * q, k, v: [B, L, H, D] of rank r; k_amax: [B, H, slots(L,64)];
- * gathered_qb: [P, B, H, 2]; v_scale: [B, H, D]; send: [P, chunk_bytes]. */
+ * gathered_qb: [P, B, H, 2]; v_scale: [B, H, D]; send: [P, chunk_bytes],
+ * zero-filled here first so the alignment padding of every chunk is zero. */
 void orc_pack(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *k_mean,
               int dtype, const float *k_amax, const float *gathered_qb, const float *v_scale,
               int B, int L, int H, int D, int rank, int world_size, uint8_t *send)
@@ -341,6 +343,7 @@ void orc_pack(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uin
     const int fk = first_group(rank, L, GK);
     size_t oq, ok, ov, oqs, oks, cb;
     orc_chunk_layout(B, L, h, D, &oq, &ok, &ov, &oqs, &oks, &cb);
+    memset(send, 0, (size_t)P * cb);
 
     float *qs = malloc(sizeof(float) * (size_t)nq);   /* per-slot scales of one (b, H) */
     float *ks = malloc(sizeof(float) * (size_t)nk);

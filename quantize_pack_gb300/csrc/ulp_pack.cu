@@ -147,6 +147,15 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a)
     }
     if (jq == tq - 1) {                                  // slots past the touched groups
         const int t = threadIdx.x;
+        if (b == a.B - 1 && j == a.h - 1) {
+            // this CTA is the last writer of the chunk's scale sections: zero
+            // their alignment padding so every chunk byte is defined
+            const size_t nqs = (size_t)a.B * a.h * a.nq, nks = (size_t)a.B * a.h * a.nk;
+            float *qsec = reinterpret_cast<float *>(chunk + a.lay.qs);
+            float *ksec = reinterpret_cast<float *>(chunk + a.lay.ks);
+            if (nqs + t < (a.lay.ks - a.lay.qs) / 4) qsec[nqs + t] = 0.0f;
+            if (nks + t < (a.lay.bytes - a.lay.ks) / 4) ksec[nks + t] = 0.0f;
+        }
         if (tq + t < a.nq) qs_out[tq + t] = __fdiv_rn(kEps, 127.0f);
         if (tk + t < a.nk) {
             float kam;
