@@ -94,6 +94,15 @@ __device__ __forceinline__ uint4 ld_stream(const void *p)
     return r;
 }
 
+// 16-byte asynchronous global -> shared copy (completes at cp_async_wait_all).
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
+{
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ float warp_max(float v)
 {
 #pragma unroll
@@ -117,10 +126,10 @@ __device__ __forceinline__ int int8_code(float y)
 }
 
 // Pack four int codes (low byte of each) into one word, first in the lowest byte.
-__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
+__device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
-    uint32_t lo = __byte_perm((uint32_t)a, (uint32_t)b, 0x0040);
-    uint32_t hi = __byte_perm((uint32_t)c, (uint32_t)d, 0x0040);
+    uint32_t lo = __byte_perm(a, b, 0x0040);
+    uint32_t hi = __byte_perm(c, d, 0x0040);
     return __byte_perm(lo, hi, 0x5410);
 }
 
@@ -128,6 +137,130 @@ __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
 __device__ __forceinline__ uint32_t e4m3x2(float x, float y)
 {
     return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x, y), __NV_SATFINITE, __NV_E4M3);
+}
+
+// ---------------------------------------------------------------------------
+// Exact quantisation of x / s by bracketing.
+//
+// The codes are those of the IEEE quotient z = rn(x / s).  Let r = rn(1/s)
+// (__frcp_rn) and r_lo = rn(r (1 - 2^-22)), r_hi = rn(r (1 + 2^-22)).  Each of
+// the three roundings in x * r_lo (and x * r_hi) is within 2^-24 relative, as
+// is z's own, so for x != 0 the exact products x * r_lo and x * r_hi lie
+// strictly on either side of z (for x < 0 the sides swap), with a bracket
+// narrower than 2^-20 |x / s|.  Both the int8 code (round half to even, then
+// saturate) and the E4M3 code (RNE, satfinite) are monotone in their input, so
+// when the two bracket ends give the same code, z gives it too.  Otherwise --
+// z near a rounding boundary, about 2^-14 of the values -- the code is taken
+// from the IEEE quotient __fdiv_rn(x, s).
+//
+// int8: fma(x, r, 1.5 * 2^23) rounds the exact product to an integer (ties to
+// even) in one step while |x r| < 2^22: the sum lies in the binade of unit
+// spacing.  With |x| <= rn(127.25 s) the quotient is below 127.5 in magnitude,
+// so no saturation applies and the code is the sum's low byte.
+// E4M3: both ends are rounded products (one more rounding each), so the V
+// brackets use the wider margin 2^-21.
+constexpr float kRoundMagic = 12582912.0f;   // 1.5 * 2^23
+constexpr float kBracketLo = 0.999999761581420898f;   // 1 - 2^-22
+constexpr float kBracketHi = 1.000000238418579102f;   // 1 + 2^-22
+constexpr float kBracketLoV = 0.999999523162841797f;  // 1 - 2^-21
+constexpr float kBracketHiV = 1.000000476837158203f;  // 1 + 2^-21
+
+struct Int8Scale {
+    float s, lo, hi, xlim;   // scale, bracketing reciprocals, largest |x| without saturation
+};
+
+__device__ __forceinline__ Int8Scale int8_scale(float s)
+{
+    const float r = __frcp_rn(s);
+    return Int8Scale{s, __fmul_rn(r, kBracketLo), __fmul_rn(r, kBracketHi), __fmul_rn(127.25f, s)};
+}
+
+// Eight int8 codes of x[e] / s, packed little-endian into two words.
+__device__ __forceinline__ uint2 int8_codes8(const float (&x)[8], const Int8Scale &q)
+{
+    uint32_t t[8];
+    bool ok = true;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float a = __fmaf_rn(x[e], q.lo, kRoundMagic);
+        const float b = __fmaf_rn(x[e], q.hi, kRoundMagic);
+        ok &= (a == b) & (fabsf(x[e]) <= q.xlim);
+        t[e] = __float_as_uint(a);
+    }
+    if (!ok) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t[e] = (uint32_t)int8_code(__fdiv_rn(x[e], q.s));
+    }
+    return make_uint2(pack4(t[0], t[1], t[2], t[3]), pack4(t[4], t[5], t[6], t[7]));
+}
+
+// Eight E4M3 codes of x[e] / s[e] given the bracketing reciprocals of s[e]
+// (e4m3_brackets), packed little-endian into two words.
+__device__ __forceinline__ uint2 e4m3_codes8(const float (&x)[8], const float (&s)[8],
+                                             const float (&rl)[8], const float (&rh)[8])
+{
+    uint32_t w[4];
+    bool ok = true;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t lo = e4m3x2(__fmul_rn(x[2 * e], rl[2 * e]), __fmul_rn(x[2 * e + 1], rl[2 * e + 1]));
+        const uint32_t hi = e4m3x2(__fmul_rn(x[2 * e], rh[2 * e]), __fmul_rn(x[2 * e + 1], rh[2 * e + 1]));
+        ok &= lo == hi;
+        w[e] = lo;
+    }
+    if (!ok) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            w[e] = e4m3x2(__fdiv_rn(x[2 * e], s[2 * e]), __fdiv_rn(x[2 * e + 1], s[2 * e + 1]));
+    }
+    return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+}
+
+// Bracketing reciprocals of a V scale for e4m3_codes8.
+__device__ __forceinline__ void e4m3_brackets(float s, float &rl, float &rh)
+{
+    const float r = __frcp_rn(s);
+    rl = __fmul_rn(r, kBracketLoV);
+    rh = __fmul_rn(r, kBracketHiV);
+}
+
+// ------------------------------------------------- packed 16-bit min / max
+
+// Per-lane running max and min of 16-bit floating-point pairs (exact).
+template <int DT>
+struct Pair16 {
+    uint32_t mx, mn;
+    __device__ __forceinline__ void init()
+    {
+        mx = DT == ULP_BF16 ? 0xFF80FF80u : 0xFC00FC00u;   // -inf, -inf
+        mn = DT == ULP_BF16 ? 0x7F807F80u : 0x7C007C00u;   // +inf, +inf
+    }
+    __device__ __forceinline__ void add(uint32_t w)
+    {
+        if (DT == ULP_BF16) {
+            const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&w);
+            __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&mx), b = *reinterpret_cast<__nv_bfloat162 *>(&mn);
+            a = __hmax2(a, v);
+            b = __hmin2(b, v);
+            mx = *reinterpret_cast<uint32_t *>(&a);
+            mn = *reinterpret_cast<uint32_t *>(&b);
+        } else {
+            const __half2 v = *reinterpret_cast<const __half2 *>(&w);
+            __half2 a = *reinterpret_cast<__half2 *>(&mx), b = *reinterpret_cast<__half2 *>(&mn);
+            a = __hmax2(a, v);
+            b = __hmin2(b, v);
+            mx = *reinterpret_cast<uint32_t *>(&a);
+            mn = *reinterpret_cast<uint32_t *>(&b);
+        }
+    }
+};
+
+// fp32 values of the two halves of a 16-bit pair word (low half first).
+template <int DT>
+__device__ __forceinline__ float2 pair_f32(uint32_t w)
+{
+    if (DT == ULP_BF16) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
 }
 
 }  // namespace ulp

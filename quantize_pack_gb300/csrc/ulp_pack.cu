@@ -3,12 +3,15 @@
 // all-to-all moves (page "unpack_for_sage": recv_u8 is the source-major
 // buffer of chunks; Returns: the V scale remains with the caller).
 //
-// One CTA handles one 128-row global Q group (a "slab") of one head on one
-// rank: Q, K and V rows of the slab are loaded once into registers, the Q
-// amax and the amax of the slab's two 64-row K groups are reduced in the CTA,
-// and the codes are written from the same registers.  Boundary groups (the
-// rank's first/last touched group) take their amax from the gathered partials
-// (Q) or the derived slots (K), so every input byte crosses HBM once.
+// Work unit: a "slab" = one 128-row global Q group of one head on one rank,
+// one CTA each.  Q and K rows are loaded once into registers, V rows into
+// shared memory; the Q amax and the amax of the slab's two 64-row K groups are
+// reduced in the CTA and the codes are written from the same registers.
+// Boundary groups (the rank's first/last touched group) take their amax from
+// the gathered partials (Q) or the derived slots (K), so every input byte
+// crosses HBM once.  Quotients use a correctly rounded reciprocal with an
+// exact fallback near rounding boundaries (ulp_internal.cuh), so the codes are
+// those of the IEEE quotient.
 #include "ulp_internal.cuh"
 
 namespace ulp {
@@ -23,188 +26,292 @@ struct PackArgs {
     int B, L, H, P, h, rank, used, fused, layout, nq, nk;
 };
 
-template <int D, int DT>
-__global__ void __launch_bounds__(256) pack_kernel(PackArgs a)
+constexpr int kPackThreads = 512;
+
+template <int D>
+struct PackSmem {
+    uint4 vtile[kGQ * D / 8];                 // V rows of the slab
+    float red[kPackThreads / 32][3];          // per-warp Q, K0, K1 maxima
+    Int8Scale scl[3];                         // Q, K group 0, K group 1
+    float vs[D], vl[D], vh[D];                // V channel scales and bracketing reciprocals
+};
+
+struct Slab {
+    int rk, r, b, hh, jq, g, L, S, row0, tq, fk, lk, tk, gu;
+};
+
+// One slab: FULL = all 128 rows belong to the rank and none is excluded from
+// the K amax (so no per-row predicate is needed).
+template <int D, int DT, bool FULL>
+__device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, PackSmem<D> &sm)
 {
-    constexpr int NV = D / 8;        // 16-byte vectors per row
-    constexpr int RL = 256 / NV;     // row lanes
-    constexpr int IT = kGQ / RL;     // rows per thread
+    constexpr int NV = D / 8;                 // 16-byte vectors per row
+    constexpr int RL = kPackThreads / NV;     // row lanes
+    constexpr int IT = kGQ / RL;              // rows per thread
+    constexpr int NW = kPackThreads / 32;
     static_assert(IT % 2 == 0 && RL * IT / 2 == kGK, "slab halves must be the K groups");
 
-    int blk = blockIdx.x;
-    const int hh = blk % a.H; blk /= a.H;
-    const int jq = blk % a.nq; blk /= a.nq;
-    const int b = blk % a.B; blk /= a.B;
-    const int rk = blk;
-    const int r = a.rank >= 0 ? a.rank : rk;
-    const int L = a.L, S = a.P * L, row0 = r * L;
-    const int fq = first_group(r, L, kGQ), tq = last_group(r, L, kGQ) - fq + 1;
-    if (jq >= tq) return;
-    const int fk = first_group(r, L, kGK), lk = last_group(r, L, kGK), tk = lk - fk + 1;
-    const int g = fq + jq;
     const int c = threadIdx.x % NV, rl = threadIdx.x / NV;
-    const int gu = a.used < S ? (a.used - 1) / kGK : -1;
+    const int L = sl.L, row0 = sl.row0, g = sl.g;
     const size_t HD = (size_t)a.H * D;
-    const size_t in_off = (size_t)rk * a.B * L * HD + (size_t)b * L * HD + (size_t)hh * D + c * 8;
+    const int t_first = g * kGQ + rl;                 // row i is t_first + i * RL
+    // global row t of this rank lives at in_base + t * HD
+    const size_t in_base = ((size_t)sl.rk * a.B + sl.b) * L * HD - (size_t)row0 * HD + (size_t)sl.hh * D + c * 8;
+    auto valid = [&](int t) { return FULL || (t >= row0 && t < row0 + L); };
 
-    // ---- load the slab (rows of this rank only)
-    uint4 qv[IT], kv[IT], vv[IT];
+    // ---- 1. V rows -> shared memory
 #pragma unroll
     for (int i = 0; i < IT; ++i) {
-        const int t = g * kGQ + i * RL + rl;
-        if (t >= row0 && t < row0 + L) {
-            const size_t o = in_off + (size_t)(t - row0) * HD;
-            qv[i] = ld_stream(a.q + o);
-            kv[i] = ld_stream(a.k + o);
-            vv[i] = ld_stream(a.v + o);
+        const int t = t_first + i * RL;
+        if (valid(t)) cp_async16(&sm.vtile[(i * RL + rl) * NV + c], a.v + in_base + (size_t)t * HD);
+    }
+    cp_async_commit();
+
+    // ---- 2. Q, K rows -> registers; V channel scales
+    uint4 qv[IT], kv[IT];
+#pragma unroll
+    for (int i = 0; i < IT; ++i) {
+        const int t = t_first + i * RL;
+        if (valid(t)) {
+            qv[i] = ld_stream(a.q + in_base + (size_t)t * HD);
+            kv[i] = ld_stream(a.k + in_base + (size_t)t * HD);
         }
+    }
+    if (threadIdx.x < D) {
+        const float s = a.v_scale[((size_t)sl.b * a.H + sl.hh) * D + threadIdx.x];
+        sm.vs[threadIdx.x] = s;
+        e4m3_brackets(s, sm.vl[threadIdx.x], sm.vh[threadIdx.x]);
     }
     float m[8];
-    to_f32x8<DT>(*reinterpret_cast<const uint4 *>(a.k_mean + ((size_t)b * a.H + hh) * D + c * 8), m);
+    to_f32x8<DT>(*reinterpret_cast<const uint4 *>(a.k_mean + ((size_t)sl.b * a.H + sl.hh) * D + c * 8), m);
 
-    // ---- amax of the slab: Q over all its rows, K per 64-row half
+    // ---- 3. amax: Q over all rows of the slab, K per 64-row half.  Per
+    // channel pair, a running max and min of the raw 16-bit values (exact);
+    // then max |Q| = max(maxQ, -minQ) and, rn subtraction being monotone,
+    // max |rn(K - m)| = max(rn(maxK - m), rn(m - minK)).
     float qmax = -INFINITY, kmax0 = -INFINITY, kmax1 = -INFINITY;
+    {
+        Pair16<DT> pr[4];
 #pragma unroll
-    for (int i = 0; i < IT; ++i) {
-        const int t = g * kGQ + i * RL + rl;
-        if (t >= row0 && t < row0 + L) {
-            float f[8];
-            to_f32x8<DT>(qv[i], f);
+        for (int x = 0; x < 4; ++x) pr[x].init();
 #pragma unroll
-            for (int x = 0; x < 8; ++x) qmax = fmaxf(qmax, fabsf(f[x]));
-            if (!(t >= a.used && t / kGK == gu)) {           // live rows only in the partial group
-                to_f32x8<DT>(kv[i], f);
-                float km = -INFINITY;
-#pragma unroll
-                for (int x = 0; x < 8; ++x) km = fmaxf(km, fabsf(__fsub_rn(f[x], m[x])));
-                if (i < IT / 2) kmax0 = fmaxf(kmax0, km);
-                else kmax1 = fmaxf(kmax1, km);
+        for (int i = 0; i < IT; ++i) {
+            if (valid(t_first + i * RL)) {
+                pr[0].add(qv[i].x);
+                pr[1].add(qv[i].y);
+                pr[2].add(qv[i].z);
+                pr[3].add(qv[i].w);
             }
         }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const float2 hi = pair_f32<DT>(pr[x].mx), lo = pair_f32<DT>(pr[x].mn);
+            qmax = fmaxf(qmax, fmaxf(fmaxf(hi.x, -lo.x), fmaxf(hi.y, -lo.y)));
+        }
     }
-    __shared__ float red[8][3];
+#pragma unroll
+    for (int hk = 0; hk < 2; ++hk) {
+        Pair16<DT> pr[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) pr[x].init();
+#pragma unroll
+        for (int i = hk * IT / 2; i < (hk + 1) * IT / 2; ++i) {
+            const int t = t_first + i * RL;
+            // live rows only in the partial live group
+            if (FULL || (valid(t) && !(t >= a.used && t / kGK == sl.gu))) {
+                pr[0].add(kv[i].x);
+                pr[1].add(kv[i].y);
+                pr[2].add(kv[i].z);
+                pr[3].add(kv[i].w);
+            }
+        }
+        float v = -INFINITY;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const float2 hi = pair_f32<DT>(pr[x].mx), lo = pair_f32<DT>(pr[x].mn);
+            v = fmaxf(v, fmaxf(fmaxf(__fsub_rn(hi.x, m[2 * x]), __fsub_rn(m[2 * x], lo.x)),
+                               fmaxf(__fsub_rn(hi.y, m[2 * x + 1]), __fsub_rn(m[2 * x + 1], lo.y))));
+        }
+        if (hk == 0) kmax0 = v;
+        else kmax1 = v;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     qmax = warp_max(qmax);
     kmax0 = warp_max(kmax0);
     kmax1 = warp_max(kmax1);
-    const int warp = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) {
-        red[warp][0] = qmax;
-        red[warp][1] = kmax0;
-        red[warp][2] = kmax1;
+    if (lane == 0) {
+        sm.red[warp][0] = qmax;
+        sm.red[warp][1] = kmax0;
+        sm.red[warp][2] = kmax1;
     }
     __syncthreads();
-    qmax = red[0][0];
-    kmax0 = red[0][1];
-    kmax1 = red[0][2];
-#pragma unroll
-    for (int w = 1; w < 8; ++w) {
-        qmax = fmaxf(qmax, red[w][0]);
-        kmax0 = fmaxf(kmax0, red[w][1]);
-        kmax1 = fmaxf(kmax1, red[w][2]);
-    }
 
-    // ---- scales
-    float qam;
-    if (jq == 0 || jq == tq - 1) {                      // boundary: merge the gathered partials
-        const int rend = min(g * kGQ + kGQ, S);
-        qam = -INFINITY;
-        for (int rr = (g * kGQ) / L; rr <= (rend - 1) / L; ++rr) {
-            const int ee = g == first_group(rr, L, kGQ) ? 0 : 1;
-            qam = fmaxf(qam, a.qpart[(((size_t)rr * a.B + b) * a.H + hh) * 2 + ee]);
+    const size_t amax_row = (((size_t)sl.rk * a.B + sl.b) * a.H + sl.hh) * a.nk;
+    if (warp == 0) {
+        qmax = lane < NW ? sm.red[lane][0] : -INFINITY;
+        kmax0 = lane < NW ? sm.red[lane][1] : -INFINITY;
+        kmax1 = lane < NW ? sm.red[lane][2] : -INFINITY;
+        qmax = warp_max(qmax);
+        kmax0 = warp_max(kmax0);
+        kmax1 = warp_max(kmax1);
+        if (lane == 0) {
+            float qam;
+            if (sl.jq == 0 || sl.jq == sl.tq - 1) {         // boundary: merge the gathered partials
+                const int rend = min(g * kGQ + kGQ, sl.S);
+                qam = -INFINITY;
+                for (int rr = (g * kGQ) / L; rr <= (rend - 1) / L; ++rr) {
+                    const int ee = g == first_group(rr, L, kGQ) ? 0 : 1;
+                    qam = fmaxf(qam, a.qpart[(((size_t)rr * a.B + sl.b) * a.H + sl.hh) * 2 + ee]);
+                }
+            } else {
+                qam = floor_eps(qmax);
+            }
+            sm.scl[0] = int8_scale(__fdiv_rn(qam, 127.0f));
+        } else if (lane == 1 || lane == 2) {
+            const int hk = lane - 1, gk = 2 * g + hk;
+            float ks = 1.0f;
+            if (gk >= sl.fk && gk <= sl.lk) {
+                const int jk = gk - sl.fk;
+                float kam;
+                if (jk == 0 || jk == sl.tk - 1 || !a.fused) {
+                    kam = a.k_amax[amax_row + jk];
+                } else {
+                    kam = floor_eps(hk == 0 ? kmax0 : kmax1);
+                    a.k_amax[amax_row + jk] = kam;
+                }
+                ks = __fdiv_rn(kam, 127.0f);
+            }
+            sm.scl[1 + hk] = int8_scale(ks);
         }
-    } else {
-        qam = floor_eps(qmax);
     }
-    const float qs = __fdiv_rn(qam, 127.0f);
-    const size_t amax_row = (((size_t)rk * a.B + b) * a.H + hh) * a.nk;
-    float ks[2] = {1.0f, 1.0f};
-#pragma unroll
-    for (int hk = 0; hk < 2; ++hk) {
-        const int gk = 2 * g + hk;
-        if (gk < fk || gk > lk) continue;
-        const int jk = gk - fk;
-        float kam;
-        if (jk == 0 || jk == tk - 1 || !a.fused) {
-            kam = a.k_amax[amax_row + jk];
-        } else {
-            kam = floor_eps(hk == 0 ? kmax0 : kmax1);
-            if (threadIdx.x == 0) a.k_amax[amax_row + jk] = kam;
-        }
-        ks[hk] = __fdiv_rn(kam, 127.0f);
-    }
+    __syncthreads();
 
-    const int p = hh / a.h, j = hh % a.h;
+    // ---- scale slots of the chunk
+    const int p = sl.hh / a.h, j = sl.hh - p * a.h;
     const size_t cb = a.lay.bytes;
     uint8_t *chunk = a.send + (a.layout == ULP_SEND_DEST_MAJOR
-                                   ? ((size_t)p * a.P + r) * cb
-                                   : ((size_t)(a.rank >= 0 ? 0 : rk) * a.P + p) * cb);
-    float *qs_out = reinterpret_cast<float *>(chunk + a.lay.qs) + ((size_t)b * a.h + j) * a.nq;
-    float *ks_out = reinterpret_cast<float *>(chunk + a.lay.ks) + ((size_t)b * a.h + j) * a.nk;
-    if (threadIdx.x == 0) qs_out[jq] = qs;
-    if (threadIdx.x == 1 || threadIdx.x == 2) {
-        const int gk = 2 * g + (threadIdx.x - 1);
-        if (gk >= fk && gk <= lk) ks_out[gk - fk] = ks[threadIdx.x - 1];
-    }
-    if (jq == tq - 1) {                                  // slots past the touched groups
+                                   ? ((size_t)p * a.P + sl.r) * cb
+                                   : ((size_t)(a.rank >= 0 ? 0 : sl.rk) * a.P + p) * cb);
+    if (threadIdx.x < 32) {
+        float *qs_out = reinterpret_cast<float *>(chunk + a.lay.qs) + ((size_t)sl.b * a.h + j) * a.nq;
+        float *ks_out = reinterpret_cast<float *>(chunk + a.lay.ks) + ((size_t)sl.b * a.h + j) * a.nk;
         const int t = threadIdx.x;
-        if (b == a.B - 1 && j == a.h - 1) {
-            // this CTA is the last writer of the chunk's scale sections: zero
-            // their alignment padding so every chunk byte is defined
-            const size_t nqs = (size_t)a.B * a.h * a.nq, nks = (size_t)a.B * a.h * a.nk;
-            float *qsec = reinterpret_cast<float *>(chunk + a.lay.qs);
-            float *ksec = reinterpret_cast<float *>(chunk + a.lay.ks);
-            if (nqs + t < (a.lay.ks - a.lay.qs) / 4) qsec[nqs + t] = 0.0f;
-            if (nks + t < (a.lay.bytes - a.lay.ks) / 4) ksec[nks + t] = 0.0f;
+        if (t == 0) qs_out[sl.jq] = sm.scl[0].s;
+        if (t == 1 || t == 2) {
+            const int gk = 2 * g + (t - 1);
+            if (gk >= sl.fk && gk <= sl.lk) ks_out[gk - sl.fk] = sm.scl[t].s;
         }
-        if (tq + t < a.nq) qs_out[tq + t] = __fdiv_rn(kEps, 127.0f);
-        if (tk + t < a.nk) {
-            float kam;
-            if (a.fused) {
-                kam = kEps;
-                a.k_amax[amax_row + tk + t] = kam;
-            } else {
-                kam = a.k_amax[amax_row + tk + t];
+        if (sl.jq == sl.tq - 1) {                        // slots past the touched groups
+            if (sl.b == a.B - 1 && j == a.h - 1) {
+                // the last writer of the chunk's scale sections zeroes their
+                // alignment padding, so every chunk byte is defined
+                const size_t nqs = (size_t)a.B * a.h * a.nq, nks = (size_t)a.B * a.h * a.nk;
+                float *qsec = reinterpret_cast<float *>(chunk + a.lay.qs);
+                float *ksec = reinterpret_cast<float *>(chunk + a.lay.ks);
+                if (nqs + t < (a.lay.ks - a.lay.qs) / 4) qsec[nqs + t] = 0.0f;
+                if (nks + t < (a.lay.bytes - a.lay.ks) / 4) ksec[nks + t] = 0.0f;
             }
-            ks_out[tk + t] = __fdiv_rn(kam, 127.0f);
+            if (sl.tq + t < a.nq) qs_out[sl.tq + t] = __fdiv_rn(kEps, 127.0f);
+            if (sl.tk + t < a.nk) {
+                float kam;
+                if (a.fused) {
+                    kam = kEps;
+                    a.k_amax[amax_row + sl.tk + t] = kam;
+                } else {
+                    kam = a.k_amax[amax_row + sl.tk + t];
+                }
+                ks_out[sl.tk + t] = __fdiv_rn(kam, 127.0f);
+            }
         }
     }
 
-    // ---- quantise from registers and store 8 bytes per row and tensor
-    float vs[8];
-    {
-        const float4 *vp = reinterpret_cast<const float4 *>(a.v_scale + ((size_t)b * a.H + hh) * D + c * 8);
-        const float4 v0 = vp[0], v1 = vp[1];
-        vs[0] = v0.x; vs[1] = v0.y; vs[2] = v0.z; vs[3] = v0.w;
-        vs[4] = v1.x; vs[5] = v1.y; vs[6] = v1.z; vs[7] = v1.w;
-    }
+    // ---- 4. Q codes, then K codes, from registers (8 bytes per row)
     const size_t hD = (size_t)a.h * D;
+    // global row t of this rank goes to out_base + t * hD within a section
+    uint8_t *out_base = chunk + ((size_t)sl.b * L - row0) * hD + (size_t)j * D + c * 8;
+    {
+        const Int8Scale qsc = sm.scl[0];
 #pragma unroll
-    for (int i = 0; i < IT; ++i) {
-        const int t = g * kGQ + i * RL + rl;
-        if (t >= row0 && t < row0 + L) {
-            const size_t o = ((size_t)b * L + (t - row0)) * hD + (size_t)j * D + c * 8;
-            float f[8];
-            int cq[8];
-            to_f32x8<DT>(qv[i], f);
-#pragma unroll
-            for (int x = 0; x < 8; ++x) cq[x] = int8_code(__fdiv_rn(f[x], qs));
-            *reinterpret_cast<uint2 *>(chunk + a.lay.q + o) =
-                make_uint2(pack4(cq[0], cq[1], cq[2], cq[3]), pack4(cq[4], cq[5], cq[6], cq[7]));
-            const float ksr = i < IT / 2 ? ks[0] : ks[1];
-            to_f32x8<DT>(kv[i], f);
-#pragma unroll
-            for (int x = 0; x < 8; ++x) cq[x] = int8_code(__fdiv_rn(__fsub_rn(f[x], m[x]), ksr));
-            *reinterpret_cast<uint2 *>(chunk + a.lay.k + o) =
-                make_uint2(pack4(cq[0], cq[1], cq[2], cq[3]), pack4(cq[4], cq[5], cq[6], cq[7]));
-            to_f32x8<DT>(vv[i], f);
-            uint32_t w[4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x)
-                w[x] = e4m3x2(__fdiv_rn(f[2 * x], vs[2 * x]), __fdiv_rn(f[2 * x + 1], vs[2 * x + 1]));
-            *reinterpret_cast<uint2 *>(chunk + a.lay.v + o) =
-                make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+        for (int i = 0; i < IT; ++i) {
+            const int t = t_first + i * RL;
+            if (valid(t)) {
+                float f[8];
+                to_f32x8<DT>(qv[i], f);
+                *reinterpret_cast<uint2 *>(out_base + (size_t)t * hD + a.lay.q) = int8_codes8(f, qsc);
+            }
         }
     }
+    to_f32x8<DT>(*reinterpret_cast<const uint4 *>(a.k_mean + ((size_t)sl.b * a.H + sl.hh) * D + c * 8), m);
+#pragma unroll
+    for (int hk = 0; hk < 2; ++hk) {
+        const Int8Scale ksc = sm.scl[1 + hk];
+#pragma unroll
+        for (int i = hk * IT / 2; i < (hk + 1) * IT / 2; ++i) {
+            const int t = t_first + i * RL;
+            if (valid(t)) {
+                float f[8];
+                to_f32x8<DT>(kv[i], f);
+#pragma unroll
+                for (int x = 0; x < 8; ++x) f[x] = __fsub_rn(f[x], m[x]);
+                *reinterpret_cast<uint2 *>(out_base + (size_t)t * hD + a.lay.k) = int8_codes8(f, ksc);
+            }
+        }
+    }
+
+    // ---- 5. V codes from shared memory (rows this thread copied itself)
+    float vs[8], vl[8], vh[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+        vs[x] = sm.vs[c * 8 + x];
+        vl[x] = sm.vl[c * 8 + x];
+        vh[x] = sm.vh[c * 8 + x];
+    }
+    cp_async_wait_all();
+#pragma unroll
+    for (int i = 0; i < IT; ++i) {
+        const int t = t_first + i * RL;
+        if (valid(t)) {
+            float f[8];
+            to_f32x8<DT>(sm.vtile[(i * RL + rl) * NV + c], f);
+            *reinterpret_cast<uint2 *>(out_base + (size_t)t * hD + a.lay.v) = e4m3_codes8(f, vs, vl, vh);
+        }
+    }
+}
+
+// One CTA per slab (blockIdx = head, slab index, rank * B + batch).
+//  1. V rows of the slab -> shared memory with cp.async (each thread later
+//     reads back only the bytes it copied, so no barrier guards them);
+//  2. Q and K rows -> registers; V channel scales and their bracketing
+//     reciprocals -> shared memory (one reciprocal per channel);
+//  3. Q amax and the amax of the two 64-row K groups: per-thread, per-warp,
+//     then warp 0 merges the warps, applies the boundary rules and publishes
+//     the scales;
+//  4. Q/K codes from the registers; 5. V codes from shared memory.
+template <int D, int DT>
+__global__ void __launch_bounds__(kPackThreads, 2) pack_kernel(PackArgs a)
+{
+    __shared__ __align__(16) PackSmem<D> sm;
+    Slab sl;
+    sl.hh = blockIdx.x;
+    sl.jq = blockIdx.y;
+    sl.rk = blockIdx.z / a.B;
+    sl.b = blockIdx.z - sl.rk * a.B;
+    sl.r = a.rank >= 0 ? a.rank : sl.rk;
+    sl.L = a.L;
+    sl.S = a.P * a.L;
+    sl.row0 = sl.r * a.L;
+    const int fq = first_group(sl.r, a.L, kGQ);
+    sl.tq = last_group(sl.r, a.L, kGQ) - fq + 1;
+    if (sl.jq >= sl.tq) return;
+    sl.g = fq + sl.jq;
+    sl.fk = first_group(sl.r, a.L, kGK);
+    sl.lk = last_group(sl.r, a.L, kGK);
+    sl.tk = sl.lk - sl.fk + 1;
+    sl.gu = a.used < sl.S ? (a.used - 1) / kGK : -1;
+    const bool full = sl.g * kGQ >= sl.row0 && sl.g * kGQ + kGQ <= sl.row0 + a.L &&
+                      !(sl.gu >= 0 && sl.gu / 2 == sl.g);
+    if (full) pack_slab<D, DT, true>(a, sl, sm);
+    else pack_slab<D, DT, false>(a, sl, sm);
 }
 
 }  // namespace ulp
@@ -233,15 +340,17 @@ extern "C" int ulp_pack(const void *q, const void *k, const void *v, const void 
     // A shard touches at least ceil(L/G) groups, so at most one slot per
     // (b, head) is untouched; the last slab's CTA writes it.
     const int nranks = rank == ULP_ALL_RANKS ? world_size : 1;
-    const long long blocks = (long long)nranks * B * a.nq * H;
-    if (blocks > INT_MAX) return fail(ULP_EINVAL, "pack: grid of %lld blocks", blocks);
+    if (a.nq > 65535 || (long long)nranks * B > 65535)
+        return fail(ULP_EINVAL, "pack: grid too large (slots %d, ranks x batch %lld)", a.nq,
+                    (long long)nranks * B);
+    const dim3 grid((unsigned)H, (unsigned)a.nq, (unsigned)(nranks * B));
     const cudaStream_t st = (cudaStream_t)stream;
     if (D == 128) {
-        if (dtype == ULP_BF16) pack_kernel<128, ULP_BF16><<<(unsigned)blocks, 256, 0, st>>>(a);
-        else pack_kernel<128, ULP_FP16><<<(unsigned)blocks, 256, 0, st>>>(a);
+        if (dtype == ULP_BF16) pack_kernel<128, ULP_BF16><<<grid, kPackThreads, 0, st>>>(a);
+        else pack_kernel<128, ULP_FP16><<<grid, kPackThreads, 0, st>>>(a);
     } else {
-        if (dtype == ULP_BF16) pack_kernel<64, ULP_BF16><<<(unsigned)blocks, 256, 0, st>>>(a);
-        else pack_kernel<64, ULP_FP16><<<(unsigned)blocks, 256, 0, st>>>(a);
+        if (dtype == ULP_BF16) pack_kernel<64, ULP_BF16><<<grid, kPackThreads, 0, st>>>(a);
+        else pack_kernel<64, ULP_FP16><<<grid, kPackThreads, 0, st>>>(a);
     }
     return check_launch("pack");
 }
