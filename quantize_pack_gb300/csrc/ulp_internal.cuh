@@ -4,7 +4,6 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -133,11 +132,6 @@ __device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, ui
     return __byte_perm(lo, hi, 0x5410);
 }
 
-// Two fp32 -> two E4M3 bytes (x in the low byte), round to nearest even, satfinite.
-__device__ __forceinline__ uint32_t e4m3x2(float x, float y)
-{
-    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x, y), __NV_SATFINITE, __NV_E4M3);
-}
 
 // ---------------------------------------------------------------------------
 // Exact quantisation of x / s by bracketing.
@@ -175,23 +169,39 @@ __device__ __forceinline__ Int8Scale int8_scale(float s)
     return Int8Scale{s, __fmul_rn(r, kBracketLo), __fmul_rn(r, kBracketHi), __fmul_rn(127.25f, s)};
 }
 
-// Eight int8 codes of x[e] / s, packed little-endian into two words.
+// Eight int8 codes of x[e] / s, packed little-endian into two words.  The two
+// bracket ends agree iff their bit patterns do; the range test folds |x| by
+// max.  (NaN inputs are outside the domain: fmaxf drops them.)
 __device__ __forceinline__ uint2 int8_codes8(const float (&x)[8], const Int8Scale &q)
 {
-    uint32_t t[8];
-    bool ok = true;
+    uint32_t t[8], diff = 0;
+    float xm = 0.0f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-        const float a = __fmaf_rn(x[e], q.lo, kRoundMagic);
-        const float b = __fmaf_rn(x[e], q.hi, kRoundMagic);
-        ok &= (a == b) & (fabsf(x[e]) <= q.xlim);
-        t[e] = __float_as_uint(a);
+        const uint32_t a = __float_as_uint(__fmaf_rn(x[e], q.lo, kRoundMagic));
+        const uint32_t b = __float_as_uint(__fmaf_rn(x[e], q.hi, kRoundMagic));
+        diff |= a ^ b;
+        xm = fmaxf(xm, fabsf(x[e]));
+        t[e] = a;
     }
-    if (!ok) {
+    if (diff != 0 || !(xm <= q.xlim)) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) t[e] = (uint32_t)int8_code(__fdiv_rn(x[e], q.s));
     }
     return make_uint2(pack4(t[0], t[1], t[2], t[3]), pack4(t[4], t[5], t[6], t[7]));
+}
+
+// Four fp32 -> four E4M3 bytes (a in the lowest byte), RNE, satfinite.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
+{
+    uint32_t w;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(w)
+        : "f"(a), "f"(b), "f"(c), "f"(d));
+    return w;
 }
 
 // Eight E4M3 codes of x[e] / s[e] given the bracketing reciprocals of s[e]
@@ -199,21 +209,26 @@ __device__ __forceinline__ uint2 int8_codes8(const float (&x)[8], const Int8Scal
 __device__ __forceinline__ uint2 e4m3_codes8(const float (&x)[8], const float (&s)[8],
                                              const float (&rl)[8], const float (&rh)[8])
 {
-    uint32_t w[4];
-    bool ok = true;
+    uint32_t w[2], diff = 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const uint32_t lo = e4m3x2(__fmul_rn(x[2 * e], rl[2 * e]), __fmul_rn(x[2 * e + 1], rl[2 * e + 1]));
-        const uint32_t hi = e4m3x2(__fmul_rn(x[2 * e], rh[2 * e]), __fmul_rn(x[2 * e + 1], rh[2 * e + 1]));
-        ok &= lo == hi;
+    for (int e = 0; e < 2; ++e) {
+        const int o = 4 * e;
+        const uint32_t lo = e4m3x4(__fmul_rn(x[o], rl[o]), __fmul_rn(x[o + 1], rl[o + 1]),
+                                   __fmul_rn(x[o + 2], rl[o + 2]), __fmul_rn(x[o + 3], rl[o + 3]));
+        const uint32_t hi = e4m3x4(__fmul_rn(x[o], rh[o]), __fmul_rn(x[o + 1], rh[o + 1]),
+                                   __fmul_rn(x[o + 2], rh[o + 2]), __fmul_rn(x[o + 3], rh[o + 3]));
+        diff |= lo ^ hi;
         w[e] = lo;
     }
-    if (!ok) {
+    if (diff != 0) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            w[e] = e4m3x2(__fdiv_rn(x[2 * e], s[2 * e]), __fdiv_rn(x[2 * e + 1], s[2 * e + 1]));
+        for (int e = 0; e < 2; ++e) {
+            const int o = 4 * e;
+            w[e] = e4m3x4(__fdiv_rn(x[o], s[o]), __fdiv_rn(x[o + 1], s[o + 1]),
+                          __fdiv_rn(x[o + 2], s[o + 2]), __fdiv_rn(x[o + 3], s[o + 3]));
+        }
     }
-    return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+    return make_uint2(w[0], w[1]);
 }
 
 // Bracketing reciprocals of a V scale for e4m3_codes8.
