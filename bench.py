@@ -56,6 +56,42 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# ------------------------------------------------------- recorded traffic
+
+PACK_SOURCES = ["quantize_pack_gb300/csrc/ulp_pack.cu", "quantize_pack_gb300/csrc/ulp_internal.cuh"]
+TRAFFIC_PROFILE = "profiles/pack_kernel_long_nonaligned.md"
+
+
+def pack_source_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in PACK_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload_name):
+    """DRAM bytes (read + write) per pack launch from the committed ncu
+    summary, or None when it was taken on other kernel sources or another
+    workload."""
+    path = os.path.join(ROOT, TRAFFIC_PROFILE)
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    fields[k.strip().strip("`- ")] = v.strip().strip("`")
+        if fields.get("source_sha256") != pack_source_digest():
+            return None
+        if fields.get("workload") != workload_name:
+            return None
+        return int(fields["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -182,6 +218,25 @@ def run_reference(args, wl, rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ multi-rank
+
+def max_over_ranks(dist, values, device=None):
+    """Element-wise max of a list of floats over every rank (identity when
+    dist is None).  The bench's timings are the slowest rank's."""
+    if dist is None:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_value(step_bytes, world, ms):
+    """Whole-job effective bandwidth in GB/s: every rank's bytes over the
+    slowest rank's time per step."""
+    return step_bytes * world / (ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def run_ours(args, wl, rank, world, dist):
@@ -249,10 +304,7 @@ def run_ours(args, wl, rank, world, dist):
 
     ms = start.elapsed_time(end) / K
     pack_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev_pack)
-    if dist is not None:
-        t = torch.tensor([ms, pack_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, pack_ms = float(t[0]), float(t[1])
+    ms, pack_ms = max_over_ranks(dist, [ms, pack_ms], dev)
 
     # ---- end to end through the public API with host buffers
     E = max(1, args.e2e_steps)
@@ -280,17 +332,14 @@ def run_ours(args, wl, rank, world, dist):
     ee.record(stream)
     torch.cuda.synchronize()
     e2e_ms = es.elapsed_time(ee) / E
-    if dist is not None:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    (e2e_ms,) = max_over_ranks(dist, [e2e_ms], dev)
     h2d = sum(t.numel() * t.element_size() for t in (pin["q"], pin["k"], pin["v"], km_p, vs_p))
     d2h = sum(t.numel() * t.element_size() for t in outs_h)
 
     if rank != 0:
         return
     step_bytes = metrics.step_bytes(wl)
-    value = step_bytes * world / (ms * 1e-3) / 1e9
+    value = whole_job_value(step_bytes, world, ms)
     peak, peak_kind = peaks()
     pack_gbs = metrics.pack_bytes(wl) / (pack_ms * 1e-3) / 1e9
     line = {
@@ -309,10 +358,10 @@ def run_ours(args, wl, rank, world, dist):
         "step_bytes": step_bytes,
         "roofline": {"bound": "hbm", "kernel": "pack_kernel", "achieved": pack_gbs, "peak": peak,
                      "peak_kind": f"{peak_kind} (STREAM copy)", "unit": "GB/s",
-                     "frac": pack_gbs / peak, "traffic": None,
+                     "frac": pack_gbs / peak, "traffic": recorded_traffic(wl.name),
                      "algorithmic_bytes_per_launch": metrics.pack_bytes(wl),
                      "launch_ms": pack_ms},
-        "e2e": {"value": step_bytes * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": whole_job_value(step_bytes, world, e2e_ms), "unit": "GB/s",
                 "ms_per_step": e2e_ms, "steps": E, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": K * path.launches_per_step,
