@@ -41,8 +41,14 @@ USED64 = configs.Workload("used_mult64_P4_L100", B=1, H=4, D=128, P=4, L=100, dt
                           seed=15, pad_rows=16, scale_to_used=True, k_mean_std=2.0,
                           k_noise_std=0.2, outlier_frac=0.01)
 
+# one live row; an odd batch with several heads per destination at D = 64
+USED1 = configs.Workload("used1_P4_L50", B=1, H=8, D=64, P=4, L=50, dtype=configs.BF16, seed=16,
+                         pad_rows=199, scale_to_used=True, k_mean_std=4.0, k_noise_std=0.05)
+B3 = configs.Workload("b3_P2_L300_D64_fp16", B=3, H=6, D=64, P=2, L=300, dtype=configs.FP16,
+                      seed=17, pad_rows=45, k_mean_std=3.0, k_noise_std=0.1, qv_dist="t3")
+
 CPU_WORKLOADS = [TINY, PADDING_R, VIDEO_R, LONG_R, HEAVY_R, SPAN4, SPAN4_PAD, L1, CROSS_PAD, SIX,
-                 USED64]
+                 USED64, USED1, B3]
 
 
 def f32(bits: np.ndarray, dtype: int) -> np.ndarray:
