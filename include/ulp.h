@@ -33,8 +33,18 @@
  *    ULP_ECUDA reports a launch failure (cudaGetLastError after the launch).
  *    ulp_last_error() returns a message for the calling thread's last failure.
  *  - Optional integers use -1 for "None": used_sequence, scale_sequence,
- *    aligned (-1 None, 0 False, 1 True), enable_pdl (-1 select by device
- *    support, 0 off, 1 on; accepted and validated, launches are plain).
+ *    aligned (-1 None, 0 False, 1 True).
+ *  - enable_pdl (Programmatic Dependent Launch, pages "k_grouped_amax" and
+ *    "unpack_for_sage", Parameters): -1 = on where the device supports it
+ *    (compute capability >= 9), 0 = off, 1 = on, 2 = on and, for ulp_pack
+ *    only, the kernel may read q, k, v, k_mean and v_scale before the
+ *    preceding kernel on the stream has completed (the caller guarantees that
+ *    kernel does not write them).  With PDL a kernel may start while its
+ *    predecessor finishes; every kernel of this library waits for its
+ *    predecessor's completion before reading anything the predecessor may
+ *    write and before its own first global write, so chains of these calls
+ *    stay ordered.  ulp_boundary_minmax and ulp_derive_k_boundary_amax launch
+ *    without PDL.
  *  - world_size is 2, 4, 6 or 8 (6: structurally supported, not validated by
  *    the method's authors); head_dim D is 64 or 128; H % world_size == 0.
  *  - rank is in [0, world_size), or ULP_ALL_RANKS: one launch covers every

@@ -29,6 +29,8 @@ template <int D, int DT>
 __global__ void __launch_bounds__(128) k_grouped_amax_kernel(AmaxArgs a)
 {
     constexpr int NV = D / 8, RL = 128 / NV, IT = kGK / RL;
+    pdl_trigger();
+    pdl_wait();
     int blk = blockIdx.x;
     const int j = blk % a.nslots; blk /= a.nslots;
     const int hh = blk % a.H; blk /= a.H;
@@ -88,6 +90,8 @@ template <int D, int DT>
 __global__ void __launch_bounds__(128) boundary_minmax_kernel(MinmaxArgs a)
 {
     constexpr int NV = D / 8, RL = 128 / NV, ITK = kGK / RL, ITQ = kGQ / RL;
+    pdl_trigger();
+    pdl_wait();
     int blk = blockIdx.x;
     const int e = blk & 1; blk >>= 1;
     const int hh = blk % a.H; blk /= a.H;
@@ -191,6 +195,8 @@ struct DeriveArgs {
 template <int D, int DT>
 __global__ void __launch_bounds__(128) derive_kernel(DeriveArgs a)
 {
+    pdl_trigger();
+    pdl_wait();
     int blk = blockIdx.x;
     const int e = blk & 1; blk >>= 1;
     const int hh = blk % a.H; blk /= a.H;
@@ -251,7 +257,8 @@ int ulp_k_grouped_amax(const void *k, const void *k_mean, int dtype, int B, int 
                slots(L, kGK), used_sequence < 0 ? L * world_size : used_sequence};
     unsigned grid = 0;
     if (int s = grid_of((long long)nranks * B * H * a.nslots, &grid, "k_grouped_amax")) return s;
-    ULP_DISPATCH(D, dtype, (k_grouped_amax_kernel<kD, kDT><<<grid, 128, 0, (cudaStream_t)stream>>>(a)));
+    const bool pdl = pdl_enabled(enable_pdl);
+    ULP_DISPATCH(D, dtype, (launch_kernel(k_grouped_amax_kernel<kD, kDT>, dim3(grid), dim3(128), (cudaStream_t)stream, pdl, a)));
     return check_launch("k_grouped_amax");
 }
 
@@ -267,7 +274,7 @@ int ulp_boundary_minmax(const void *k, const void *q, int dtype, int B, int L, i
                  used_sequence < 0 ? L * world_size : used_sequence};
     unsigned grid = 0;
     if (int s = grid_of((long long)nranks * B * H * 2, &grid, "boundary_minmax")) return s;
-    ULP_DISPATCH(D, dtype, (boundary_minmax_kernel<kD, kDT><<<grid, 128, 0, (cudaStream_t)stream>>>(a)));
+    ULP_DISPATCH(D, dtype, (launch_kernel(boundary_minmax_kernel<kD, kDT>, dim3(grid), dim3(128), (cudaStream_t)stream, false, a)));
     return check_launch("boundary_minmax");
 }
 
@@ -284,7 +291,7 @@ int ulp_derive_k_boundary_amax(float *grouped_amax, const float *gathered_minmax
                  slots(L, kGK)};
     unsigned grid = 0;
     if (int s = grid_of((long long)nranks * B * H * 2, &grid, "derive_k_boundary_amax")) return s;
-    ULP_DISPATCH(D, dtype, (derive_kernel<kD, kDT><<<grid, kD, 0, (cudaStream_t)stream>>>(a)));
+    ULP_DISPATCH(D, dtype, (launch_kernel(derive_kernel<kD, kDT>, dim3(grid), dim3(kD), (cudaStream_t)stream, false, a)));
     return check_launch("derive_k_boundary_amax");
 }
 

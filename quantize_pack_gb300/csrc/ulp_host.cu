@@ -54,12 +54,27 @@ int check_common(int dtype, int B, int L, int H, int D, int rank, int world_size
     const int S = L * world_size;
     if (used_sequence != -1 && (used_sequence < 1 || used_sequence > S))
         return fail(ULP_EINVAL, "used_sequence %d outside [1, %d]", used_sequence, S);
-    if (enable_pdl < -1 || enable_pdl > 1)
-        return fail(ULP_EINVAL, "enable_pdl must be -1, 0 or 1 (got %d)", enable_pdl);
+    if (enable_pdl < -1 || enable_pdl > 2)
+        return fail(ULP_EINVAL, "enable_pdl must be -1, 0, 1 or 2 (got %d)", enable_pdl);
     // every per-rank tensor must stay addressable with 64-bit offsets and every
     // grid within int range
     if ((double)B * S * H * D > 4.0e15) return fail(ULP_EINVAL, "tensor too large");
     return ULP_OK;
+}
+
+bool pdl_enabled(int enable_pdl)
+{
+    if (enable_pdl >= 1) return true;
+    if (enable_pdl == 0) return false;
+    static int cached[64];   // per device: 0 unknown, 1 no, 2 yes
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (cached[dev] == 0) {
+        int major = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cached[dev] = major >= 9 ? 2 : 1;
+    }
+    return cached[dev] == 2;
 }
 
 }  // namespace ulp

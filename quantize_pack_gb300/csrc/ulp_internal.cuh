@@ -62,6 +62,41 @@ int check_common(int dtype, int B, int L, int H, int D, int rank, int world_size
                  int used_sequence, int enable_pdl);
 int check_world(int world_size);
 
+// ------------------------------------------ programmatic dependent launch
+//
+// enable_pdl: -1 = on when the device supports it (compute capability >= 9),
+// 0 = off, 1 = on, 2 = on and the pack kernel may read its inputs (q, k, v,
+// k_mean, v_scale) before the preceding kernel on the stream completes (the
+// caller guarantees that kernel does not write them).  Every kernel here lets
+// its dependents launch as soon as all its CTAs have started
+// (griddepcontrol.launch_dependents) and waits for its predecessor's
+// completion (griddepcontrol.wait) before any read of a buffer the
+// predecessor may write and before its first global write; without a
+// programmatic launch both instructions are no-ops.
+bool pdl_enabled(int enable_pdl);
+
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch a kernel taking one argument struct, optionally as a programmatic
+// dependent launch.
+template <typename Args>
+cudaError_t launch_kernel(void (*kernel)(Args), dim3 grid, dim3 block, cudaStream_t stream, bool pdl,
+                          const Args &args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args);
+}
+
 // ------------------------------------------------------------ device side
 
 // 8 consecutive bf16/fp16 values (one 16-byte vector) -> fp32, exactly.

@@ -24,6 +24,7 @@ struct PackArgs {
     uint8_t *send;
     ChunkLayout lay;
     int B, L, H, P, h, rank, used, fused, layout, nq, nk;
+    int early;   // read q, k, v, k_mean, v_scale before waiting for the preceding kernel
 };
 
 constexpr int kPackThreads = 512;
@@ -58,6 +59,7 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
     // global row t of this rank lives at in_base + t * HD
     const size_t in_base = ((size_t)sl.rk * a.B + sl.b) * L * HD - (size_t)row0 * HD + (size_t)sl.hh * D + c * 8;
     auto valid = [&](int t) { return FULL || (t >= row0 && t < row0 + L); };
+    if (!a.early) pdl_wait();
 
     // ---- 1. V rows -> shared memory
 #pragma unroll
@@ -136,6 +138,7 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
         else kmax1 = v;
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (a.early) pdl_wait();          // k_amax, the partials and the chunks belong to the chain
     qmax = warp_max(qmax);
     kmax0 = warp_max(kmax0);
     kmax1 = warp_max(kmax1);
@@ -291,6 +294,7 @@ template <int D, int DT>
 __global__ void __launch_bounds__(kPackThreads, 2) pack_kernel(PackArgs a)
 {
     __shared__ __align__(16) PackSmem<D> sm;
+    pdl_trigger();
     Slab sl;
     sl.hh = blockIdx.x;
     sl.jq = blockIdx.y;
@@ -302,7 +306,10 @@ __global__ void __launch_bounds__(kPackThreads, 2) pack_kernel(PackArgs a)
     sl.row0 = sl.r * a.L;
     const int fq = first_group(sl.r, a.L, kGQ);
     sl.tq = last_group(sl.r, a.L, kGQ) - fq + 1;
-    if (sl.jq >= sl.tq) return;
+    if (sl.jq >= sl.tq) {
+        pdl_wait();
+        return;
+    }
     sl.g = fq + sl.jq;
     sl.fk = first_group(sl.r, a.L, kGK);
     sl.lk = last_group(sl.r, a.L, kGK);
@@ -345,12 +352,14 @@ extern "C" int ulp_pack(const void *q, const void *k, const void *v, const void 
                     (long long)nranks * B);
     const dim3 grid((unsigned)H, (unsigned)a.nq, (unsigned)(nranks * B));
     const cudaStream_t st = (cudaStream_t)stream;
+    const bool pdl = pdl_enabled(enable_pdl);
+    a.early = enable_pdl == 2;
     if (D == 128) {
-        if (dtype == ULP_BF16) pack_kernel<128, ULP_BF16><<<grid, kPackThreads, 0, st>>>(a);
-        else pack_kernel<128, ULP_FP16><<<grid, kPackThreads, 0, st>>>(a);
+        if (dtype == ULP_BF16) launch_kernel(pack_kernel<128, ULP_BF16>, grid, dim3(kPackThreads), st, pdl, a);
+        else launch_kernel(pack_kernel<128, ULP_FP16>, grid, dim3(kPackThreads), st, pdl, a);
     } else {
-        if (dtype == ULP_BF16) pack_kernel<64, ULP_BF16><<<grid, kPackThreads, 0, st>>>(a);
-        else pack_kernel<64, ULP_FP16><<<grid, kPackThreads, 0, st>>>(a);
+        if (dtype == ULP_BF16) launch_kernel(pack_kernel<64, ULP_BF16>, grid, dim3(kPackThreads), st, pdl, a);
+        else launch_kernel(pack_kernel<64, ULP_FP16>, grid, dim3(kPackThreads), st, pdl, a);
     }
     return check_launch("pack");
 }

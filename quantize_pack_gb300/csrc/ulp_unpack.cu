@@ -90,6 +90,8 @@ __device__ __forceinline__ void unpack_v_tile(const UnpackArgs &a, long long til
 template <int D>
 __global__ void __launch_bounds__(kUnpackThreads) unpack_kernel(UnpackArgs a)
 {
+    pdl_trigger();
+    pdl_wait();
     long long blk = blockIdx.x;
     if (blk < a.nVblk) {
         const long long tile = blk * (kUnpackThreads / 32) + (threadIdx.x >> 5);
@@ -165,7 +167,7 @@ extern "C" int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int
     if (aligned < -1 || aligned > 1) return fail(ULP_EINVAL, "unpack: aligned must be -1, 0 or 1");
     if (aligned == 1 && L % 128 != 0)
         return fail(ULP_EINVAL, "unpack: aligned=True requires local_sequence %% 128 == 0 (L = %d)", L);
-    if (enable_pdl < -1 || enable_pdl > 1) return fail(ULP_EINVAL, "unpack: enable_pdl must be -1, 0 or 1");
+    if (enable_pdl < -1 || enable_pdl > 2) return fail(ULP_EINVAL, "unpack: enable_pdl must be -1, 0, 1 or 2");
     if ((long long)L * world_size > INT_MAX / 2) return fail(ULP_EINVAL, "unpack: sequence too long");
     const int S = L * world_size;
     if (scale_sequence != -1 && (scale_sequence < 1 || scale_sequence > S))
@@ -194,7 +196,8 @@ extern "C" int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int
     const long long blocks = a.nVblk + a.nCblk + a.nSblk;
     if (blocks > INT_MAX) return fail(ULP_EINVAL, "unpack: grid of %lld blocks", blocks);
     const cudaStream_t st = (cudaStream_t)stream;
-    if (D == 128) unpack_kernel<128><<<(unsigned)blocks, kUnpackThreads, 0, st>>>(a);
-    else unpack_kernel<64><<<(unsigned)blocks, kUnpackThreads, 0, st>>>(a);
+    const bool pdl = pdl_enabled(enable_pdl);
+    if (D == 128) launch_kernel(unpack_kernel<128>, dim3((unsigned)blocks), dim3(kUnpackThreads), st, pdl, a);
+    else launch_kernel(unpack_kernel<64>, dim3((unsigned)blocks), dim3(kUnpackThreads), st, pdl, a);
     return check_launch("unpack_for_sage");
 }

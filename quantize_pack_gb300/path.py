@@ -1,6 +1,10 @@
 """The whole quantize -> pack -> exchange -> unpack path of an emulated Ulysses
 group of P ranks held on one GPU.
 
+Pack is a programmatic dependent launch: it loads its inputs while derive
+finishes (derive writes none of them).  ``capture`` records one step as a
+CUDA graph.
+
 All P shards sit in device memory; the stats all-gather is the stacked
 [P, ...] buffer the boundary kernel writes, and the all-to-all is folded into
 the pack's store addresses (dest-major send buffer = every destination's
@@ -22,7 +26,7 @@ class UlyssesLowpPath:
     def __init__(self, *, B: int, L: int, H: int, D: int, world_size: int, dtype: torch.dtype,
                  used_sequence: Optional[int] = None, scale_sequence: Optional[int] = None,
                  aligned: Optional[bool] = None, fused: bool = True, fold_exchange: bool = True,
-                 device="cuda"):
+                 pdl: Optional[bool] = None, pdl_unpack: Optional[bool] = None, device="cuda"):
         P = world_size
         self.B, self.L, self.H, self.D, self.P = B, L, H, D, P
         self.h = H // P
@@ -33,6 +37,12 @@ class UlyssesLowpPath:
         self.aligned = aligned
         self.fused = fused
         self.fold_exchange = fold_exchange
+        # pdl: programmatic launch of pack, which follows derive (derive writes
+        # none of pack's inputs, so pack loads them before waiting);
+        # pdl_unpack: of unpack (default off: its early CTAs would sit on SMs
+        # through pack's last wave)
+        self.pdl_pack = 2 if pdl is None or pdl else 0
+        self.pdl = bool(pdl_unpack)
         self.device = torch.device(device)
         self.chunk_bytes = ulp.chunk_bytes(B, L, self.h, D)
         f32 = dict(dtype=torch.float32, device=self.device)
@@ -72,11 +82,11 @@ class UlyssesLowpPath:
         if self.fold_exchange:
             ulp.pack(q, k, v, k_mean, self.k_amax, self.q_partial, v_scale, rank=None,
                      world_size=P, used_sequence=self.used_sequence, fused=self.fused,
-                     send=self.recv, send_layout=ulp.SEND_DEST_MAJOR)
+                     send=self.recv, send_layout=ulp.SEND_DEST_MAJOR, enable_pdl=self.pdl_pack)
         else:
             ulp.pack(q, k, v, k_mean, self.k_amax, self.q_partial, v_scale, rank=None,
                      world_size=P, used_sequence=self.used_sequence, fused=self.fused,
-                     send=self.send, send_layout=ulp.SEND_SOURCE_MAJOR)
+                     send=self.send, send_layout=ulp.SEND_SOURCE_MAJOR, enable_pdl=self.pdl_pack)
         if on_pack is not None:
             on_pack[1]()
         if not self.fold_exchange:
@@ -84,7 +94,22 @@ class UlyssesLowpPath:
         return ulp.unpack_for_sage(self.recv, batch_size=self.B, local_sequence=L,
                                    local_heads=self.h, head_dim=self.D, world_size=P,
                                    aligned=self.aligned, scale_sequence=self.scale_sequence,
-                                   out=self.out)
+                                   out=self.out, enable_pdl=self.pdl)
+
+    def capture(self, q, k, v, k_mean, v_scale):
+        """Record one step on these input tensors as a CUDA graph; replay it
+        with ``graph.replay()`` after refilling the same tensors.  The outputs
+        are ``self.out``."""
+        torch.cuda.synchronize(self.device)
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            self.run(q, k, v, k_mean, v_scale)        # warm the caches of the lazy loader
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.run(q, k, v, k_mean, v_scale)
+        return graph
 
 
 def P_copies(P: int) -> int:

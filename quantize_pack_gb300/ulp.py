@@ -87,6 +87,18 @@ def _tri(x: Optional[bool]) -> int:
     return -1 if x is None else int(bool(x))
 
 
+def _pdl(x) -> int:
+    """enable_pdl: None -> -1 (by device support), False/True -> 0/1, or 2 (pack
+    may read its inputs before the preceding kernel completes)."""
+    if x is None:
+        return -1
+    if isinstance(x, bool):
+        return int(x)
+    if int(x) in (0, 1, 2):
+        return int(x)
+    raise ValueError(f"enable_pdl must be None, a bool or 2, got {x!r}")
+
+
 def _dtype_code(t: torch.Tensor) -> int:
     if t.dtype == torch.bfloat16:
         return ULP_BF16
@@ -156,7 +168,7 @@ def k_grouped_amax(k: torch.Tensor, k_mean_global: torch.Tensor, *, rank: Option
     if out is None:
         out = torch.empty(shape, dtype=torch.float32, device=k.device)
     _check(lib().ulp_k_grouped_amax(_ptr(k), _ptr(k_mean_global), _dtype_code(k), B, L, H, D, rc,
-                                    world_size, _opt(used_sequence), _ptr(out), _tri(enable_pdl),
+                                    world_size, _opt(used_sequence), _ptr(out), _pdl(enable_pdl),
                                     _stream(k.device)))
     return out
 
@@ -198,7 +210,7 @@ def pack(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, k_mean_global: torch
          rank: Optional[int], world_size: int, used_sequence: Optional[int] = None,
          fused: bool = True, send: Optional[torch.Tensor] = None,
          send_layout: int = SEND_SOURCE_MAJOR,
-         enable_pdl: Optional[bool] = None) -> torch.Tensor:
+         enable_pdl=None) -> torch.Tensor:
     """Quantise a rank's Q/K/V into its P chunks (INT8 Q/K, FP8 E4M3 V)."""
     rc, nr, B, L, H, D = _rank_dims(q, rank)
     h = H // world_size
@@ -212,7 +224,7 @@ def pack(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, k_mean_global: torch
     _check(lib().ulp_pack(_ptr(q), _ptr(k), _ptr(v), _ptr(k_mean_global), _dtype_code(q),
                           _ptr(k_amax), _ptr(gathered_q_partial), _ptr(v_scale), B, L, H, D, rc,
                           world_size, _opt(used_sequence), int(bool(fused)), _ptr(send),
-                          int(send_layout), _tri(enable_pdl), _stream(q.device)))
+                          int(send_layout), _pdl(enable_pdl), _stream(q.device)))
     return send
 
 
@@ -261,6 +273,6 @@ def unpack_for_sage(recv_u8: torch.Tensor, *, batch_size: int, local_sequence: i
     _check(lib().ulp_unpack_for_sage(_ptr(recv_u8), batch_size, local_sequence, local_heads,
                                      head_dim, world_size, _tri(aligned), _opt(scale_sequence),
                                      _ptr(q8), _ptr(k8), _ptr(v8b), _ptr(qs), _ptr(ks),
-                                     1 if nd is None else nd, _tri(enable_pdl),
+                                     1 if nd is None else nd, _pdl(enable_pdl),
                                      _stream(recv_u8.device)))
     return tuple(out)

@@ -110,3 +110,36 @@ def test_non_default_stream_and_changing_inputs():
         side.synchronize()
         for i, name in enumerate(["q8", "k8", "v8", "q_scale", "k_scale"]):
             gh.assert_bits_equal(outs[i], np.stack([res["out"][p][i] for p in range(wl.P)]), name)
+
+
+@pytest.mark.parametrize("pdl", [False, True], ids=["pdl_off", "pdl_on"])
+def test_programmatic_launch_on_and_off(pdl):
+    wl = hp.PADDING_R
+    inp, res, (q, k, v, km, vs) = _setup(wl)
+    path = UlyssesLowpPath(B=wl.B, L=wl.L, H=wl.H, D=wl.D, world_size=wl.P,
+                           dtype=gh.torch_dtype(wl.dtype), used_sequence=wl.used_sequence,
+                           scale_sequence=wl.scale_sequence, pdl=pdl)
+    for _ in range(3):
+        outs = path.run(q, k, v, km, vs)
+    torch.cuda.synchronize()
+    for i, name in enumerate(["q8", "k8", "v8", "q_scale", "k_scale"]):
+        gh.assert_bits_equal(outs[i], np.stack([res["out"][p][i] for p in range(wl.P)]), name)
+
+
+def test_cuda_graph_replay_with_new_inputs():
+    wl = hp.SIX
+    path = UlyssesLowpPath(B=wl.B, L=wl.L, H=wl.H, D=wl.D, world_size=wl.P,
+                           dtype=gh.torch_dtype(wl.dtype), used_sequence=wl.used_sequence,
+                           scale_sequence=wl.scale_sequence)
+    inp0 = synth.make_inputs(wl)
+    q, k, v, km, vs = gh.to_device(inp0)
+    graph = path.capture(q, k, v, km, vs)
+    for seed in (31, 32):
+        inp = synth.make_inputs(wl.replace(seed=seed, name=f"{wl.name}_g{seed}"))
+        res = hp.run_oracle(inp)
+        for dst, src in zip((q, k, v, km, vs), gh.to_device(inp)):
+            dst.copy_(src)
+        graph.replay()
+        torch.cuda.synchronize()
+        for i, name in enumerate(["q8", "k8", "v8", "q_scale", "k_scale"]):
+            gh.assert_bits_equal(path.out[i], np.stack([res["out"][p][i] for p in range(wl.P)]), name)
