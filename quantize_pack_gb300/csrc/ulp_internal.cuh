@@ -204,6 +204,38 @@ __device__ __forceinline__ Int8Scale int8_scale(float s)
     return Int8Scale{s, __fmul_rn(r, kBracketLo), __fmul_rn(r, kBracketHi), __fmul_rn(127.25f, s)};
 }
 
+// ---- packed fp32 pairs (Blackwell f32x2 arithmetic: two lanes per instruction)
+
+__device__ __forceinline__ unsigned long long f2pack(float a, float b)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long r, float &a, float &b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long f2fma(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c)
+{
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2mul(unsigned long long a, unsigned long long b)
+{
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2sub(unsigned long long a, unsigned long long b)
+{
+    unsigned long long r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 // Eight int8 codes of x[e] / s, packed little-endian into two words.  The two
 // bracket ends agree iff their bit patterns do; the range test folds |x| by
 // max.  (NaN inputs are outside the domain: fmaxf drops them.)
@@ -211,13 +243,18 @@ __device__ __forceinline__ uint2 int8_codes8(const float (&x)[8], const Int8Scal
 {
     uint32_t t[8], diff = 0;
     float xm = 0.0f;
+    const unsigned long long lo2 = f2pack(q.lo, q.lo), hi2 = f2pack(q.hi, q.hi);
+    const unsigned long long mg2 = f2pack(kRoundMagic, kRoundMagic);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const uint32_t a = __float_as_uint(__fmaf_rn(x[e], q.lo, kRoundMagic));
-        const uint32_t b = __float_as_uint(__fmaf_rn(x[e], q.hi, kRoundMagic));
-        diff |= a ^ b;
-        xm = fmaxf(xm, fabsf(x[e]));
-        t[e] = a;
+    for (int e = 0; e < 8; e += 2) {
+        const unsigned long long x2 = f2pack(x[e], x[e + 1]);
+        float a0, a1, b0, b1;
+        f2unpack(f2fma(x2, lo2, mg2), a0, a1);
+        f2unpack(f2fma(x2, hi2, mg2), b0, b1);
+        t[e] = __float_as_uint(a0);
+        t[e + 1] = __float_as_uint(a1);
+        diff |= (t[e] ^ __float_as_uint(b0)) | (t[e + 1] ^ __float_as_uint(b1));
+        xm = fmaxf(xm, fmaxf(fabsf(x[e]), fabsf(x[e + 1])));
     }
     if (diff != 0 || !(xm <= q.xlim)) {
 #pragma unroll
@@ -248,10 +285,15 @@ __device__ __forceinline__ uint2 e4m3_codes8(const float (&x)[8], const float (&
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
         const int o = 4 * e;
-        const uint32_t lo = e4m3x4(__fmul_rn(x[o], rl[o]), __fmul_rn(x[o + 1], rl[o + 1]),
-                                   __fmul_rn(x[o + 2], rl[o + 2]), __fmul_rn(x[o + 3], rl[o + 3]));
-        const uint32_t hi = e4m3x4(__fmul_rn(x[o], rh[o]), __fmul_rn(x[o + 1], rh[o + 1]),
-                                   __fmul_rn(x[o + 2], rh[o + 2]), __fmul_rn(x[o + 3], rh[o + 3]));
+        float l[4], h[4];
+#pragma unroll
+        for (int k = 0; k < 4; k += 2) {
+            const unsigned long long x2 = f2pack(x[o + k], x[o + k + 1]);
+            f2unpack(f2mul(x2, f2pack(rl[o + k], rl[o + k + 1])), l[k], l[k + 1]);
+            f2unpack(f2mul(x2, f2pack(rh[o + k], rh[o + k + 1])), h[k], h[k + 1]);
+        }
+        const uint32_t lo = e4m3x4(l[0], l[1], l[2], l[3]);
+        const uint32_t hi = e4m3x4(h[0], h[1], h[2], h[3]);
         diff |= lo ^ hi;
         w[e] = lo;
     }

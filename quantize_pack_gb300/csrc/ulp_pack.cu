@@ -255,7 +255,8 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
                 float f[8];
                 to_f32x8<DT>(kv[i], f);
 #pragma unroll
-                for (int x = 0; x < 8; ++x) f[x] = __fsub_rn(f[x], m[x]);
+                for (int x = 0; x < 8; x += 2)
+                    f2unpack(f2sub(f2pack(f[x], f[x + 1]), f2pack(m[x], m[x + 1])), f[x], f[x + 1]);
                 *reinterpret_cast<uint2 *>(out_base + (size_t)t * hD + a.lay.k) = int8_codes8(f, ksc);
             }
         }
