@@ -46,6 +46,38 @@ def lib():
     return _lib
 
 
+def build_variant(source: str, path: str) -> str:
+    """Compile an edited copy of oracle.c (the mutation tests plant mistakes
+    in copies to check that the pins catch them) into `path`."""
+    d = os.path.dirname(path)
+    os.makedirs(d, exist_ok=True)
+    src = os.path.join(d, "oracle_variant.c")
+    with open(src, "w") as f:
+        f.write(source)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                    "-shared", "-I", HERE, src, "-o", path, "-lm"], check=True)
+    return path
+
+
+class use_library:
+    """Context manager: route every oracle call through another build of it."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        self.saved = _lib
+        _lib = ctypes.CDLL(self.path)
+        _declare(_lib)
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SZ = ctypes.c_size_t
