@@ -57,7 +57,7 @@ FAKE = 1 << 20   # an aligned, never-dereferenced address: every call below fail
     (dict(world_size=3), -1), (dict(world_size=16), -1), (dict(rank=2, world_size=2), -1),
     (dict(rank=-2), -1), (dict(D=96), -1), (dict(H=6, world_size=4), -1),
     (dict(used=0), -1), (dict(used=2 * 96 + 1), -1), (dict(L=0), -1), (dict(B=0), -1),
-    (dict(pdl=2), -1),
+    (dict(pdl=3), -1),
     # alignment
     (dict(k=FAKE + 8), -3), (dict(k=0), -3), (dict(out=FAKE + 2), -3), (dict(km=FAKE + 4), -3),
 ])
