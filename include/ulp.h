@@ -6,6 +6,8 @@
  * sequence rows [r*L, (r+1)*L) of Q, K, V [B, L, H, D]; after the exchange a
  * destination holds all S = P*L rows of h = H/P heads.  The entry points are:
  *
+ *   ulp_k_mean_global           the step before the path: page "k_grouped_amax",
+ *                               k_mean_global parameter (the global K mean)
  *   ulp_k_grouped_amax          page "flashinfer.comm._ulysses_lowp.k_grouped_amax"
  *   ulp_boundary_minmax         page "...derive_k_boundary_amax" (gathered_minmax parameter:
  *                               the raw-K boundary min/max every rank contributes)
@@ -111,6 +113,29 @@ int ulp_chunk_bytes(int B, int L, int h, int D, size_t *chunk_bytes);
 /* Byte offsets of the five chunk sections: offsets[0..4] = Q, K, V,
  * q_scale, k_scale. */
 int ulp_chunk_offsets(int B, int L, int h, int D, size_t offsets[5]);
+
+/* Bytes of the workspace ulp_k_mean_global needs: 8 * P * B * ceil(L/512) * H * D. */
+int ulp_k_mean_workspace_bytes(int B, int L, int H, int D, int world_size, size_t *bytes);
+
+/* k_mean_global production for an emulated Ulysses group (the global K mean
+ * that page "k_grouped_amax" takes as k_mean_global: "rounded to the input
+ * dtype").  One fixed summation order, so every implementation and launch
+ * shape gives the same bits:
+ *   block sum = fp32 sum of f32(K) over the live rows (global row < used) of
+ *               a rank-local 64-row block, rows in increasing order;
+ *   partial   = fp64 pairwise sum of a rank's block sums: zero-padded to a
+ *               power of two, added in adjacent pairs level by level (the
+ *               rank's all-reduce contribution); total = fp64 sum of the
+ *               partials, ranks in order;
+ *   k_mean    = dtype(binary32(total / used)), both roundings to nearest even.
+ *   k          [P, B, L, H, D] dtype: every rank's shard
+ *   workspace  device buffer of at least ulp_k_mean_workspace_bytes bytes
+ *              (holds tree nodes; contents on return unspecified)
+ *   k_mean     [B, H, D] dtype (output)
+ * local_sequence is at most 32768 (ULP_EINVAL above). */
+int ulp_k_mean_global(const void *k, int dtype, int B, int L, int H, int D, int world_size,
+                      int used_sequence, void *workspace, size_t workspace_bytes, void *k_mean,
+                      ulp_stream_t stream);
 
 /* k_grouped_amax -- page "flashinfer.comm._ulysses_lowp.k_grouped_amax".
  * For each (b, head, slot j) of rank r:

@@ -186,6 +186,85 @@ void orc_scale_widths(int n, int *q_width, int *k_width)
     *k_width = (n + GK - 1) / GK;
 }
 
+/* ------------------------------------------------------- k_mean_global */
+
+/* k_mean_global production (the step before the path; page "k_grouped_amax",
+ * k_mean_global parameter: the global K mean, rounded to the input dtype).
+ * Reading of this library, one fixed order so that every implementation
+ * gets the same bits:
+ *   block sum  = fp32 sum of f32(K) over the live rows (t < used) of a
+ *                rank-local 64-row block [64i, 64i+64) of rank r, rows in
+ *                increasing order;
+ *   partial_r  = fp64 pairwise sum of rank r's block sums: the blocks, padded
+ *                with zeros to a power of two, are added in adjacent pairs,
+ *                level by level ((b0 + b1) + (b2 + b3)) + ... (what rank r
+ *                contributes to the all-reduce);
+ *   total      = fp64 sum of the partials, ranks in increasing order;
+ *   mean       = binary32 rounding of the fp64 quotient total / n, n = used
+ *                (S when used < 0), then rounded to the dtype (nearest even).
+ * Zero padding leaves the sums unchanged: no block sum or pair sum is -0.
+ * k_all: [P, B, L, H, D] (every rank's shard); out: [B, H, D] dtype bits. */
+static uint16_t f32_to_dtype_rne(float x, int dtype);
+
+void orc_k_mean_global(const uint16_t *k_all, int dtype, int B, int L, int H, int D,
+                       int world_size, int used, uint16_t *out)
+{
+    const int S = world_size * L;
+    const int n = used >= 0 ? used : S;
+    const int nb = (L + 63) / 64;
+    int n2 = 1;
+    while (n2 < nb) n2 *= 2;
+    double *v = malloc(sizeof(double) * (size_t)n2);
+    for (int b = 0; b < B; ++b)
+        for (int hh = 0; hh < H; ++hh)
+            for (int d = 0; d < D; ++d) {
+                double total = 0.0;
+                for (int r = 0; r < world_size; ++r) {
+                    const uint16_t *k = k_all + (size_t)r * B * L * H * D;
+                    for (int i = 0; i < n2; ++i) {
+                        float block = 0.0f;
+                        for (int tl = 64 * i; i < nb && tl < 64 * i + 64 && tl < L; ++tl) {
+                            if (r * L + tl >= n) break;                    /* live rows only */
+                            block += in_f32(k, (((size_t)b * L + tl) * H + hh) * D + d, dtype);
+                        }
+                        v[i] = (double)block;
+                    }
+                    for (int w = n2; w > 1; w /= 2)
+                        for (int i = 0; i < w / 2; ++i) v[i] = v[2 * i] + v[2 * i + 1];
+                    total += v[0];
+                }
+                const float mean = (float)(total / (double)n);
+                out[((size_t)b * H + hh) * D + d] = f32_to_dtype_rne(mean, dtype);
+            }
+    free(v);
+}
+
+/* binary32 -> bfloat16 / binary16 bits, round to nearest even (finite input;
+ * binary16 overflow gives infinity, underflow gives subnormals or zero). */
+static uint16_t f32_to_dtype_rne(float x, int dtype)
+{
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    if (dtype == ORC_BF16) {
+        uint32_t lsb = (u >> 16) & 1u;
+        return (uint16_t)((u + 0x7FFFu + lsb) >> 16);
+    }
+    /* binary16: round |x| to a multiple of its binary16 step, from the definition */
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    float a = fabsf(x);
+    if (a >= 65520.0f) return (uint16_t)(sign | 0x7C00u);   /* rounds to infinity */
+    int ex;
+    int qexp = a < 0x1p-14f ? -24 : (frexpf(a, &ex), (ex - 1) - 10);
+    float m = rne_int(ldexpf(a, -qexp));                    /* exact scaling, then round */
+    float v = ldexpf(m, qexp);
+    if (v == 0.0f) return sign;
+    if (v < 0x1p-14f) return (uint16_t)(sign | (uint16_t)m);  /* subnormal */
+    frexpf(v, &ex);
+    int E = ex - 1;
+    int mant = (int)ldexpf(v, -(E - 10)) - 1024;
+    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)mant);
+}
+
 /* ------------------------------------------------------- k_grouped_amax */
 
 /* k_grouped_amax, page "k_grouped_amax" (summary, used_sequence paragraph,

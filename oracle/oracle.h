@@ -18,6 +18,8 @@ void orc_chunk_layout(int B, int L, int h, int D, size_t *off_q, size_t *off_k, 
                       size_t *off_qs, size_t *off_ks, size_t *chunk_bytes);
 void orc_scale_widths(int n, int *q_width, int *k_width);
 
+void orc_k_mean_global(const uint16_t *k_all, int dtype, int B, int L, int H, int D,
+                       int world_size, int used, uint16_t *out);
 void orc_k_grouped_amax(const uint16_t *k, const uint16_t *k_mean, int dtype, int B, int L,
                         int H, int D, int rank, int world_size, int used, float *out);
 void orc_boundary_minmax(const uint16_t *k, const uint16_t *q, int dtype, int B, int L, int H,

@@ -100,6 +100,8 @@ def _declare(L):
     L.orc_chunk_layout.argtypes = [_I, _I, _I, _I] + [ctypes.POINTER(_SZ)] * 6
     L.orc_scale_widths.restype = None
     L.orc_scale_widths.argtypes = [_I, ctypes.POINTER(_I), ctypes.POINTER(_I)]
+    L.orc_k_mean_global.restype = None
+    L.orc_k_mean_global.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P]
     L.orc_k_grouped_amax.restype = None
     L.orc_k_grouped_amax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]
     L.orc_boundary_minmax.restype = None
@@ -166,6 +168,15 @@ def scale_widths(n: int) -> tuple:
 
 
 # ------------------------------------------------------------ path functions
+
+def k_mean_global(k_all, dtype, *, used_sequence=None):
+    """k_all: uint16 [P, B, L, H, D] -> uint16 [B, H, D] (dtype bits)."""
+    P, B, L, H, D = k_all.shape
+    out = np.empty((B, H, D), np.uint16)
+    lib().orc_k_mean_global(_ptr(k_all, np.uint16), dtype, B, L, H, D, P, _opt(used_sequence),
+                            _ptr(out, np.uint16))
+    return out
+
 
 def k_grouped_amax(k, k_mean, dtype, *, rank, world_size, used_sequence=None):
     """k: uint16 [B, L, H, D]; k_mean uint16 [B, H, D] -> float32 [B, H, slots(L,64)]."""

@@ -1,0 +1,222 @@
+// k_mean_global production: the global K mean of every (batch, head,
+// channel), rounded to the input dtype (page "k_grouped_amax", k_mean_global
+// parameter), for an emulated Ulysses group.  One fixed summation order, so
+// the bits do not depend on the launch shape:
+//   block sum = fp32 sum over the live rows of a rank-local 64-row block,
+//               rows in increasing order;
+//   partial   = fp64 pairwise sum of a rank's block sums (zero-padded to a
+//               power of two, adjacent pairs level by level): the rank's
+//               all-reduce contribution; total = fp64 sum over ranks in order;
+//   mean      = binary32 rounding of total / used, then the dtype (RNE).
+// Kernel A: a thread sums 8 consecutive blocks of 8 channels and the three
+// lowest tree levels over them, writing one fp64 node per group of 8 blocks
+// to the workspace; kernel B (one thread per channel) finishes each rank's
+// tree and the rank sum.  Reads 2 bytes per K element: HBM-bound.
+#include "ulp_internal.cuh"
+
+namespace ulp {
+
+constexpr int kMeanBlock = 64;        // rows per block sum
+constexpr int kMeanGroup = 8;         // blocks per kernel-A thread (3 tree levels)
+static_assert(kMeanGroup == 8, "kernel A builds exactly three tree levels");
+constexpr int kMeanThreads = 128;
+
+struct KMeanArgs {
+    const uint16_t *k;   // [P, B, L, H, D]
+    double *nodes;       // [P, B, ngrp, H, D]: tree nodes over 8 blocks each
+    void *out;           // [B, H, D] dtype
+    int B, L, H, D, P, nblk, ngrp, used, dtype;
+};
+
+// Kernel A: grid (ceil(H*D/4 / 128), ngrp, P * B); a thread owns 4 channels.
+template <int DT>
+__global__ void __launch_bounds__(kMeanThreads) kmean_blocks_kernel(KMeanArgs a)
+{
+    pdl_trigger();
+    pdl_wait();
+    const int HD = a.H * a.D;
+    const int vec = blockIdx.x * kMeanThreads + threadIdx.x;     // 4-channel vector of the row
+    if (vec * 4 >= HD) return;
+    const int grp = blockIdx.y;
+    const int r = blockIdx.z / a.B, b = blockIdx.z - r * a.B;
+    const int row_live = max(0, a.used - r * a.L);               // rank-local rows < this are live
+    const uint16_t *src = a.k + ((size_t)r * a.B + b) * a.L * HD + (size_t)vec * 4;
+    // The three lowest levels of the rank's pairwise tree, built as the blocks
+    // arrive: a carry stack of left children per level (lv1 holds a finished
+    // pair, lv2 a finished quad), each node = left child + right child.
+    float lv0[4];
+    double lv1[4], lv2[4], top[4];
+#pragma unroll 1
+    for (int q = 0; q < kMeanGroup; ++q) {
+        const int t0 = (grp * kMeanGroup + q) * kMeanBlock;
+        const int t1 = min(min(t0 + kMeanBlock, a.L), row_live);
+        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int t = t0; t < t1; t += 16) {
+            uint2 v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (t + i < t1) v[i] = __ldcs(reinterpret_cast<const uint2 *>(src + (size_t)(t + i) * HD));
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (t + i < t1) {
+                    const float2 lo = pair_f32<DT>(v[i].x), hi = pair_f32<DT>(v[i].y);
+                    s[0] = __fadd_rn(s[0], lo.x);                        // rows in order
+                    s[1] = __fadd_rn(s[1], lo.y);
+                    s[2] = __fadd_rn(s[2], hi.x);
+                    s[3] = __fadd_rn(s[3], hi.y);
+                }
+            }
+        }
+        if (!(q & 1)) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) lv0[x] = s[x];
+        } else {
+            double pair[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) pair[x] = __dadd_rn((double)lv0[x], (double)s[x]);
+            if (!(q & 2)) {
+#pragma unroll
+                for (int x = 0; x < 4; ++x) lv1[x] = pair[x];
+            } else {
+                double quad[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) quad[x] = __dadd_rn(lv1[x], pair[x]);
+                if (!(q & 4)) {
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) lv2[x] = quad[x];
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) top[x] = __dadd_rn(lv2[x], quad[x]);
+                }
+            }
+        }
+    }
+    double *dst = a.nodes + (((size_t)r * a.B + b) * a.ngrp + grp) * HD + (size_t)vec * 4;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) dst[x] = top[x];
+}
+
+// Kernel B: CTAs of 32 * P threads, thread (rank r, lane c) finishes rank r's
+// tree for channel 32 * blockIdx.x + c (the nodes zero-padded to a power of
+// two, added as they arrive with a carry stack of left children per level);
+// the rank-0 thread then adds the ranks in order and rounds.
+template <int DT>
+__global__ void __launch_bounds__(256) kmean_finish_kernel(KMeanArgs a)
+{
+    pdl_trigger();
+    pdl_wait();
+    __shared__ double part[8][32];
+    const int HD = a.H * a.D;
+    const int c = threadIdx.x & 31, r = threadIdx.x >> 5;
+    const long long idx = (long long)blockIdx.x * 32 + c;          // over B * HD
+    const bool live = idx < (long long)a.B * HD;
+    const int b = live ? (int)(idx / HD) : 0, ch = live ? (int)(idx - (long long)b * HD) : 0;
+    int n2 = 1;
+    while (n2 < a.ngrp) n2 *= 2;
+    double st[6];                                      // carry stack, n2 <= 64 (checked on the host)
+#pragma unroll
+    for (int l = 0; l < 6; ++l) st[l] = 0.0;
+    double root = 0.0;
+    if (live) {
+        const double *col = a.nodes + (((size_t)r * a.B + b) * a.ngrp) * HD + ch;
+        for (int i = 0; i < n2; ++i) {
+            double x = i < a.ngrp ? col[(size_t)i * HD] : 0.0;
+            // x is a node at level 0; merge with finished left siblings
+#pragma unroll
+            for (int l = 0; l < 6; ++l) {
+                if (!((i >> l) & 1)) {
+                    st[l] = x;                         // a left child waits at level l
+                    break;
+                }
+                x = __dadd_rn(st[l], x);               // left + right
+            }
+            if (i == n2 - 1) root = x;             // the last leaf completes the tree
+        }
+    }
+    part[r][c] = root;
+    __syncthreads();
+    if (r == 0 && live) {
+        double total = 0.0;
+        for (int rr = 0; rr < a.P; ++rr) total = __dadd_rn(total, part[rr][c]);
+        const float mean = __double2float_rn(__ddiv_rn(total, (double)a.used));
+        uint16_t bits;
+        if (DT == ULP_BF16) bits = __bfloat16_as_ushort(__float2bfloat16_rn(mean));
+        else bits = __half_as_ushort(__float2half_rn(mean));
+        static_cast<uint16_t *>(a.out)[idx] = bits;
+    }
+}
+
+int kmean_check(int dtype, int B, int L, int H, int D, int world_size, int used_sequence)
+{
+    if (int s = check_common(dtype, B, L, H, D, ULP_ALL_RANKS, world_size, used_sequence, -1)) return s;
+    return ULP_OK;
+}
+
+static int kmean_groups(int L)
+{
+    const int nblk = (L + kMeanBlock - 1) / kMeanBlock;
+    return (nblk + kMeanGroup - 1) / kMeanGroup;
+}
+
+size_t kmean_workspace_bytes(int B, int L, int H, int D, int world_size)
+{
+    return sizeof(double) * (size_t)world_size * B * kmean_groups(L) * H * D;
+}
+
+// Both launches on `stream`; `blocks` holds kmean_workspace_bytes bytes.
+int kmean_launch(const void *k, int dtype, int B, int L, int H, int D, int world_size,
+                 int used_sequence, double *nodes, void *k_mean, cudaStream_t stream)
+{
+    KMeanArgs a{(const uint16_t *)k, nodes, k_mean, B, L, H, D, world_size,
+                (L + kMeanBlock - 1) / kMeanBlock, kmean_groups(L),
+                used_sequence < 0 ? L * world_size : used_sequence, dtype};
+    if (a.ngrp > 64)
+        return fail(ULP_EINVAL, "k_mean_global: local_sequence %d above the %d-row maximum", L,
+                    64 * kMeanGroup * kMeanBlock);
+    const long long vecs = (long long)H * D / 4;
+    const long long gx = (vecs + kMeanThreads - 1) / kMeanThreads;
+    if (gx > INT_MAX || (long long)world_size * B > 65535)
+        return fail(ULP_EINVAL, "k_mean_global: grid too large");
+    const dim3 grid_a((unsigned)gx, (unsigned)a.ngrp, (unsigned)(world_size * B));
+    const long long nb = ((long long)B * H * D + 31) / 32;
+    if (nb > INT_MAX) return fail(ULP_EINVAL, "k_mean_global: grid too large");
+    if (dtype == ULP_BF16) {
+        launch_kernel(kmean_blocks_kernel<ULP_BF16>, grid_a, dim3(kMeanThreads), stream, false, a);
+        launch_kernel(kmean_finish_kernel<ULP_BF16>, dim3((unsigned)nb), dim3(32 * world_size), stream, false, a);
+    } else {
+        launch_kernel(kmean_blocks_kernel<ULP_FP16>, grid_a, dim3(kMeanThreads), stream, false, a);
+        launch_kernel(kmean_finish_kernel<ULP_FP16>, dim3((unsigned)nb), dim3(32 * world_size), stream, false, a);
+    }
+    return check_launch("k_mean_global");
+}
+
+}  // namespace ulp
+
+using namespace ulp;
+
+extern "C" {
+
+int ulp_k_mean_workspace_bytes(int B, int L, int H, int D, int world_size, size_t *bytes)
+{
+    if (int s = check_world(world_size)) return s;
+    if (B < 1 || L < 1 || H < 1 || (D != 64 && D != 128) || !bytes)
+        return fail(ULP_EINVAL, "k_mean_workspace_bytes: bad sizes");
+    *bytes = kmean_workspace_bytes(B, L, H, D, world_size);
+    return ULP_OK;
+}
+
+int ulp_k_mean_global(const void *k, int dtype, int B, int L, int H, int D, int world_size,
+                      int used_sequence, void *workspace, size_t workspace_bytes, void *k_mean,
+                      ulp_stream_t stream)
+{
+    if (int s = kmean_check(dtype, B, L, H, D, world_size, used_sequence)) return s;
+    if (!aligned16(k) || !aligned16(workspace) || !aligned16(k_mean))
+        return fail(ULP_EALIGN, "k_mean_global: k, workspace, k_mean must be 16-byte aligned");
+    const size_t need = kmean_workspace_bytes(B, L, H, D, world_size);
+    if (workspace_bytes < need)
+        return fail(ULP_EINVAL, "k_mean_global: workspace of %zu bytes, %zu needed", workspace_bytes, need);
+    return kmean_launch(k, dtype, B, L, H, D, world_size, used_sequence, (double *)workspace, k_mean,
+                        (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
         L.ulp_scale_widths.argtypes = [_I, ctypes.POINTER(_I), ctypes.POINTER(_I)]
         L.ulp_chunk_bytes.argtypes = [_I, _I, _I, _I, ctypes.POINTER(_SZ)]
         L.ulp_chunk_offsets.argtypes = [_I, _I, _I, _I, ctypes.POINTER(_SZ)]
+        L.ulp_k_mean_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]
+        L.ulp_k_mean_global.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _P]
         L.ulp_k_grouped_amax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P]
         L.ulp_boundary_minmax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]
         L.ulp_derive_k_boundary_amax.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]
@@ -66,6 +68,7 @@ def lib() -> ctypes.CDLL:
         L.ulp_unpack_for_sage.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I,
                                           _I, _P]
         for name in ("ulp_slots", "ulp_scale_widths", "ulp_chunk_bytes", "ulp_chunk_offsets",
+                     "ulp_k_mean_workspace_bytes", "ulp_k_mean_global",
                      "ulp_k_grouped_amax", "ulp_boundary_minmax", "ulp_derive_k_boundary_amax",
                      "ulp_pack", "ulp_alltoall_emulate", "ulp_unpack_for_sage"):
             getattr(L, name).restype = _I
@@ -155,6 +158,29 @@ def _rank_dims(x: torch.Tensor, rank: Optional[int]):
     if x.dim() != 4:
         raise ValueError("expected a shard [B, L, H, D]")
     return int(rank), 1, *x.shape
+
+
+def k_mean_workspace_bytes(B: int, L: int, H: int, D: int, world_size: int) -> int:
+    n = _SZ()
+    _check(lib().ulp_k_mean_workspace_bytes(B, L, H, D, world_size, ctypes.byref(n)))
+    return n.value
+
+
+def k_mean_global(k: torch.Tensor, *, used_sequence: Optional[int] = None,
+                  workspace: Optional[torch.Tensor] = None,
+                  out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Global K mean [B, H, D] in k's dtype from every rank's shard
+    k [P, B, L, H, D] (the all-reduce emulated in one call)."""
+    P, B, L, H, D = k.shape
+    need = k_mean_workspace_bytes(B, L, H, D, P)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=k.device)
+    if out is None:
+        out = torch.empty((B, H, D), dtype=k.dtype, device=k.device)
+    _check(lib().ulp_k_mean_global(_ptr(k), _dtype_code(k), B, L, H, D, P, _opt(used_sequence),
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _ptr(out), _stream(k.device)))
+    return out
 
 
 def k_grouped_amax(k: torch.Tensor, k_mean_global: torch.Tensor, *, rank: Optional[int],
