@@ -137,6 +137,28 @@ int ulp_k_mean_global(const void *k, int dtype, int B, int L, int H, int D, int 
                       int used_sequence, void *workspace, size_t workspace_bytes, void *k_mean,
                       ulp_stream_t stream);
 
+/* ulp_k_mean_global without a workspace.  The pages have no counterpart of
+ * this entry point; it exists for callers that cannot allocate device memory
+ * for this call -- for example code inside a host framework whose caching
+ * allocator already holds the device memory it manages, a plugin that may
+ * only touch the tensors it is handed, or a latency-bound loop where a
+ * cudaMalloc (which can synchronise the device) is not acceptable.
+ * Same arguments and results as ulp_k_mean_global minus the workspace: the
+ * tree nodes go to a fixed 8 MiB device array inside the library, which every
+ * device that loads the library holds until the library is unloaded.
+ *   - Shapes whose nodes need more than 8 MiB (8 * P * B * ceil(L/512) * H * D
+ *     bytes) are rejected with ULP_EINVAL and a message; nothing is launched.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress, that device current) and caches it; make that first
+ *     call before any stream capture on the device.
+ *   - Every call uses the same array and leaves its nodes there; each call
+ *     writes every node it reads, so no clearing is needed.  Calls whose
+ *     kernels can overlap on the GPU (other streams, other host threads) race
+ *     on the array: order them on one stream or with events. */
+int ulp_k_mean_global_noalloc(const void *k, int dtype, int B, int L, int H, int D, int world_size,
+                              int used_sequence, void *k_mean, ulp_stream_t stream);
+
 /* k_grouped_amax -- page "flashinfer.comm._ulysses_lowp.k_grouped_amax".
  * For each (b, head, slot j) of rank r:
  *   out[b,H,j] = max(1e-7, max |rn(f32(k[b,t,H,d]) - f32(k_mean[b,H,d]))|)

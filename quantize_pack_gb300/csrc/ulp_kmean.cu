@@ -220,3 +220,68 @@ int ulp_k_mean_global(const void *k, int dtype, int B, int L, int H, int D, int 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// k_mean_global without any allocation by the caller or the library.
+//
+// Some callers cannot hand this library a workspace: a host framework whose
+// caching allocator has already reserved the device memory it manages, a
+// plugin that may only touch the tensors it is given, or a latency-bound
+// loop where a cudaMalloc (which can synchronise the device) is not allowed.
+// For them the tree nodes live in one fixed, file-scope device array instead.
+// The array exists on every device that loads this library, for as long as
+// the library stays loaded, whether or not this entry point is ever called.
+
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;   // 8 MiB of tree nodes
+static __device__ __align__(256) unsigned char g_kmean_scratch[kNoAllocScratchBytes];
+
+// Device address of g_kmean_scratch per device.  Host code must not use the
+// array's name as an address: on the host it only stands in for the symbol.
+std::mutex g_scratch_mutex;
+void *g_scratch_addr[128];
+
+int scratch_address(void **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return ulp::fail(ULP_ECUDA, "k_mean_global_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 128) return ulp::fail(ULP_EINVAL, "k_mean_global_noalloc: device %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_kmean_scratch);    // with `dev` current
+        if (e != cudaSuccess || !p)
+            return ulp::fail(ULP_ECUDA, "k_mean_global_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return ULP_OK;
+}
+
+}  // namespace
+
+extern "C" int ulp_k_mean_global_noalloc(const void *k, int dtype, int B, int L, int H, int D,
+                                         int world_size, int used_sequence, void *k_mean,
+                                         ulp_stream_t stream)
+{
+    using namespace ulp;
+    if (int s = kmean_check(dtype, B, L, H, D, world_size, used_sequence)) return s;
+    if (!aligned16(k) || !aligned16(k_mean))
+        return fail(ULP_EALIGN, "k_mean_global_noalloc: k and k_mean must be 16-byte aligned");
+    const size_t need = kmean_workspace_bytes(B, L, H, D, world_size);
+    if (need > kNoAllocScratchBytes)
+        return fail(ULP_EINVAL,
+                    "k_mean_global_noalloc: this shape needs %zu bytes of scratch, the fixed "
+                    "array holds %zu; use ulp_k_mean_global with a workspace",
+                    need, kNoAllocScratchBytes);
+    void *scratch = nullptr;
+    if (int s = scratch_address(&scratch)) return s;
+    // Every tree node kernel B reads is written by kernel A of the same call,
+    // so the previous call's leftovers never need clearing.
+    return kmean_launch(k, dtype, B, L, H, D, world_size, used_sequence, (double *)scratch, k_mean,
+                        (cudaStream_t)stream);
+}

@@ -59,6 +59,7 @@ def lib() -> ctypes.CDLL:
         L.ulp_chunk_offsets.argtypes = [_I, _I, _I, _I, ctypes.POINTER(_SZ)]
         L.ulp_k_mean_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]
         L.ulp_k_mean_global.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _P]
+        L.ulp_k_mean_global_noalloc.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P]
         L.ulp_k_grouped_amax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P]
         L.ulp_boundary_minmax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]
         L.ulp_derive_k_boundary_amax.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]
@@ -68,7 +69,7 @@ def lib() -> ctypes.CDLL:
         L.ulp_unpack_for_sage.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I,
                                           _I, _P]
         for name in ("ulp_slots", "ulp_scale_widths", "ulp_chunk_bytes", "ulp_chunk_offsets",
-                     "ulp_k_mean_workspace_bytes", "ulp_k_mean_global",
+                     "ulp_k_mean_workspace_bytes", "ulp_k_mean_global", "ulp_k_mean_global_noalloc",
                      "ulp_k_grouped_amax", "ulp_boundary_minmax", "ulp_derive_k_boundary_amax",
                      "ulp_pack", "ulp_alltoall_emulate", "ulp_unpack_for_sage"):
             getattr(L, name).restype = _I
@@ -180,6 +181,21 @@ def k_mean_global(k: torch.Tensor, *, used_sequence: Optional[int] = None,
     _check(lib().ulp_k_mean_global(_ptr(k), _dtype_code(k), B, L, H, D, P, _opt(used_sequence),
                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _ptr(out), _stream(k.device)))
+    return out
+
+
+def k_mean_global_noalloc(k: torch.Tensor, *, used_sequence: Optional[int] = None,
+                          out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """k_mean_global for callers that cannot allocate device memory for the
+    call: the library keeps its intermediate sums in a fixed 8 MiB device
+    array instead of a workspace (larger shapes raise).  Pass `out` to avoid
+    any allocation on this side too.  Calls that can overlap on the GPU share
+    that array and must be ordered by the caller."""
+    P, B, L, H, D = k.shape
+    if out is None:
+        out = torch.empty((B, H, D), dtype=k.dtype, device=k.device)
+    _check(lib().ulp_k_mean_global_noalloc(_ptr(k), _dtype_code(k), B, L, H, D, P,
+                                           _opt(used_sequence), _ptr(out), _stream(k.device)))
     return out
 
 
