@@ -220,7 +220,9 @@ int ulp_derive_k_boundary_amax(float *grouped_amax, const float *gathered_minmax
  *   k_mean              [B, H, D] dtype
  *   k_amax              [B, H, slots(L,64)] fp32 ([P, ...] for ULP_ALL_RANKS)
  *   gathered_q_partial  [P, B, H, 2] fp32 (from ulp_boundary_minmax)
- *   v_scale             [B, H, D] fp32, the caller's V scale (per global head)
+ *   v_scale             [B, H, D] fp32, the caller's V scale (per global head);
+ *                       positive and at least 2^-92 (smaller scales may code
+ *                       inputs below 2^-102 with the wrong E4M3 value)
  *   send                ULP_SEND_SOURCE_MAJOR: [P, chunk_bytes] of this rank
  *                       ([P_src, P_dst, chunk_bytes] for ULP_ALL_RANKS);
  *                       ULP_SEND_DEST_MAJOR: [P_dst, P_src, chunk_bytes], the

@@ -169,40 +169,32 @@ __device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, ui
 
 
 // ---------------------------------------------------------------------------
-// Exact quantisation of x / s by bracketing.
+// Exact quantisation of x / s without a divide per element.
 //
-// The codes are those of the IEEE quotient z = rn(x / s).  Let r = rn(1/s)
-// (__frcp_rn) and r_lo = rn(r (1 - 2^-22)), r_hi = rn(r (1 + 2^-22)).  Each of
-// the three roundings in x * r_lo (and x * r_hi) is within 2^-24 relative, as
-// is z's own, so for x != 0 the exact products x * r_lo and x * r_hi lie
-// strictly on either side of z (for x < 0 the sides swap), with a bracket
-// narrower than 2^-20 |x / s|.  Both the int8 code (round half to even, then
-// saturate) and the E4M3 code (RNE, satfinite) are monotone in their input, so
-// when the two bracket ends give the same code, z gives it too.  Otherwise --
-// z near a rounding boundary, about 2^-14 of the values -- the code is taken
-// from the IEEE quotient __fdiv_rn(x, s).
+// The codes are those of the IEEE quotient z = rn(x / s).  With r = rn(1/s)
+// (__frcp_rn) and y = rn(x * r), Markstein's correction
+//     e = fma(-y, s, x),   z = fma(e, r, y)
+// gives z = rn(x / s).  Rounding to nearest commutes with scaling by powers
+// of two, so the identity depends only on the significands of x and s; it
+// was checked against __fdiv_rn for all 2^46 pairs of binary32 significands
+// (x, s in [1, 2)) with zero mismatches.  It therefore holds whenever r, y and
+// e stay normal.  e underflows only for |x| < 2^-102; then every int8 code is 0,
+// and so is every E4M3 code when s >= 2^-92, whose sign is restored from y
+// (the correction turns -0 into +0).  The only other failure is y overflowing
+// to infinity (z becomes NaN): callers that can meet it test for it (int8
+// saturating path, E4M3 path).
 //
-// int8: fma(x, r, 1.5 * 2^23) rounds the exact product to an integer (ties to
-// even) in one step while |x r| < 2^22: the sum lies in the binade of unit
-// spacing.  With |x| <= rn(127.25 s) the quotient is below 127.5 in magnitude,
-// so no saturation applies and the code is the sum's low byte.
-// E4M3: both ends are rounded products (one more rounding each), so the V
-// brackets use the wider margin 2^-21.
+// int8 code = saturate(rne(z)): rne(z) is read off z + 1.5 * 2^23 (the sum's
+// binade has unit spacing) and saturating first gives the same code.  Where
+// the scale comes from the group's own amax, |x| <= amax bounds |z| by
+// 127 (1 + 2^-23), so no saturation is needed (int8_codes8<false>).
 constexpr float kRoundMagic = 12582912.0f;   // 1.5 * 2^23
-constexpr float kBracketLo = 0.999999761581420898f;   // 1 - 2^-22
-constexpr float kBracketHi = 1.000000238418579102f;   // 1 + 2^-22
-constexpr float kBracketLoV = 0.999999523162841797f;  // 1 - 2^-21
-constexpr float kBracketHiV = 1.000000476837158203f;  // 1 + 2^-21
 
 struct Int8Scale {
-    float s, lo, hi, xlim;   // scale, bracketing reciprocals, largest |x| without saturation
+    float s, r;   // scale and rn(1/scale)
 };
 
-__device__ __forceinline__ Int8Scale int8_scale(float s)
-{
-    const float r = __frcp_rn(s);
-    return Int8Scale{s, __fmul_rn(r, kBracketLo), __fmul_rn(r, kBracketHi), __fmul_rn(127.25f, s)};
-}
+__device__ __forceinline__ Int8Scale int8_scale(float s) { return Int8Scale{s, __frcp_rn(s)}; }
 
 // ---- packed fp32 pairs (Blackwell f32x2 arithmetic: two lanes per instruction)
 
@@ -229,6 +221,12 @@ __device__ __forceinline__ unsigned long long f2mul(unsigned long long a, unsign
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
+__device__ __forceinline__ unsigned long long f2add(unsigned long long a, unsigned long long b)
+{
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
 __device__ __forceinline__ unsigned long long f2sub(unsigned long long a, unsigned long long b)
 {
     unsigned long long r;
@@ -236,29 +234,41 @@ __device__ __forceinline__ unsigned long long f2sub(unsigned long long a, unsign
     return r;
 }
 
-// Eight int8 codes of x[e] / s, packed little-endian into two words.  The two
-// bracket ends agree iff their bit patterns do; the range test folds |x| by
-// max.  (NaN inputs are outside the domain: fmaxf drops them.)
+// rn(x / s) for a pair sharing nothing: y = x * r, e = fma(-y, s, x), z = fma(e, r, y).
+__device__ __forceinline__ unsigned long long f2quot(unsigned long long x2, unsigned long long r2,
+                                                     unsigned long long ns2, unsigned long long &y2)
+{
+    y2 = f2mul(x2, r2);
+    return f2fma(f2fma(y2, ns2, x2), r2, y2);
+}
+
+// Eight int8 codes of rn(x[e] / s), packed little-endian into two words.
+// SAT = false: the caller guarantees |x| <= 127 s (1 + 2^-24), so no code
+// saturates; SAT = true: any finite x.
+template <bool SAT>
 __device__ __forceinline__ uint2 int8_codes8(const float (&x)[8], const Int8Scale &q)
 {
-    uint32_t t[8], diff = 0;
-    float xm = 0.0f;
-    const unsigned long long lo2 = f2pack(q.lo, q.lo), hi2 = f2pack(q.hi, q.hi);
+    const unsigned long long r2 = f2pack(q.r, q.r), ns2 = f2pack(-q.s, -q.s);
     const unsigned long long mg2 = f2pack(kRoundMagic, kRoundMagic);
+    uint32_t t[8];
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
-        const unsigned long long x2 = f2pack(x[e], x[e + 1]);
-        float a0, a1, b0, b1;
-        f2unpack(f2fma(x2, lo2, mg2), a0, a1);
-        f2unpack(f2fma(x2, hi2, mg2), b0, b1);
+        unsigned long long y2;
+        const unsigned long long z2 = f2quot(f2pack(x[e], x[e + 1]), r2, ns2, y2);
+        float a0, a1;
+        if (SAT) {
+            float y0, y1;
+            f2unpack(z2, a0, a1);
+            f2unpack(y2, y0, y1);
+            a0 = fabsf(y0) <= 3.4028235e38f ? a0 : y0;            // y overflowed: z is NaN
+            a1 = fabsf(y1) <= 3.4028235e38f ? a1 : y1;
+            a0 = __fadd_rn(fminf(fmaxf(a0, -128.0f), 127.0f), kRoundMagic);
+            a1 = __fadd_rn(fminf(fmaxf(a1, -128.0f), 127.0f), kRoundMagic);
+        } else {
+            f2unpack(f2add(z2, mg2), a0, a1);
+        }
         t[e] = __float_as_uint(a0);
         t[e + 1] = __float_as_uint(a1);
-        diff |= (t[e] ^ __float_as_uint(b0)) | (t[e + 1] ^ __float_as_uint(b1));
-        xm = fmaxf(xm, fmaxf(fabsf(x[e]), fabsf(x[e + 1])));
-    }
-    if (diff != 0 || !(xm <= q.xlim)) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) t[e] = (uint32_t)int8_code(__fdiv_rn(x[e], q.s));
     }
     return make_uint2(pack4(t[0], t[1], t[2], t[3]), pack4(t[4], t[5], t[6], t[7]));
 }
@@ -276,44 +286,33 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
     return w;
 }
 
-// Eight E4M3 codes of x[e] / s[e] given the bracketing reciprocals of s[e]
-// (e4m3_brackets), packed little-endian into two words.
+// Eight E4M3 codes of rn(x[e] / s[e]) given r[e] = rn(1/s[e]), packed
+// little-endian into two words.  A quotient whose first product y overflowed
+// (possible only with extreme caller scales) sends the group to __fdiv_rn.
 __device__ __forceinline__ uint2 e4m3_codes8(const float (&x)[8], const float (&s)[8],
-                                             const float (&rl)[8], const float (&rh)[8])
+                                             const float (&r)[8])
 {
-    uint32_t w[2], diff = 0;
+    float z[8];
+    float ym = 0.0f;
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int o = 4 * e;
-        float l[4], h[4];
-#pragma unroll
-        for (int k = 0; k < 4; k += 2) {
-            const unsigned long long x2 = f2pack(x[o + k], x[o + k + 1]);
-            f2unpack(f2mul(x2, f2pack(rl[o + k], rl[o + k + 1])), l[k], l[k + 1]);
-            f2unpack(f2mul(x2, f2pack(rh[o + k], rh[o + k + 1])), h[k], h[k + 1]);
-        }
-        const uint32_t lo = e4m3x4(l[0], l[1], l[2], l[3]);
-        const uint32_t hi = e4m3x4(h[0], h[1], h[2], h[3]);
-        diff |= lo ^ hi;
-        w[e] = lo;
+    for (int e = 0; e < 8; e += 2) {
+        unsigned long long y2;
+        const unsigned long long z2 = f2quot(f2pack(x[e], x[e + 1]), f2pack(r[e], r[e + 1]),
+                                             f2pack(-s[e], -s[e + 1]), y2);
+        float y0, y1;
+        f2unpack(z2, z[e], z[e + 1]);
+        f2unpack(y2, y0, y1);
+        ym = fmaxf(ym, fmaxf(fabsf(y0), fabsf(y1)));
+        // a zero quotient keeps the sign of x (y has it; the correction's
+        // +0 + -0 would not)
+        z[e] = copysignf(z[e], y0);
+        z[e + 1] = copysignf(z[e + 1], y1);
     }
-    if (diff != 0) {
+    if (!(ym <= 3.4028235e38f)) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int o = 4 * e;
-            w[e] = e4m3x4(__fdiv_rn(x[o], s[o]), __fdiv_rn(x[o + 1], s[o + 1]),
-                          __fdiv_rn(x[o + 2], s[o + 2]), __fdiv_rn(x[o + 3], s[o + 3]));
-        }
+        for (int e = 0; e < 8; ++e) z[e] = __fdiv_rn(x[e], s[e]);
     }
-    return make_uint2(w[0], w[1]);
-}
-
-// Bracketing reciprocals of a V scale for e4m3_codes8.
-__device__ __forceinline__ void e4m3_brackets(float s, float &rl, float &rh)
-{
-    const float r = __frcp_rn(s);
-    rl = __fmul_rn(r, kBracketLoV);
-    rh = __fmul_rn(r, kBracketHiV);
+    return make_uint2(e4m3x4(z[0], z[1], z[2], z[3]), e4m3x4(z[4], z[5], z[6], z[7]));
 }
 
 // ------------------------------------------------- packed 16-bit min / max

@@ -34,7 +34,7 @@ struct PackSmem {
     uint4 vtile[kGQ * D / 8];                 // V rows of the slab
     float red[kPackThreads / 32][3];          // per-warp Q, K0, K1 maxima
     Int8Scale scl[3];                         // Q, K group 0, K group 1
-    float vs[D], vl[D], vh[D];                // V channel scales and bracketing reciprocals
+    float vs[D], vr[D];                       // V channel scales and their reciprocals
 };
 
 struct Slab {
@@ -82,7 +82,7 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
     if (threadIdx.x < D) {
         const float s = a.v_scale[((size_t)sl.b * a.H + sl.hh) * D + threadIdx.x];
         sm.vs[threadIdx.x] = s;
-        e4m3_brackets(s, sm.vl[threadIdx.x], sm.vh[threadIdx.x]);
+        sm.vr[threadIdx.x] = __frcp_rn(s);
     }
     float m[8];
     to_f32x8<DT>(*reinterpret_cast<const uint4 *>(a.k_mean + ((size_t)sl.b * a.H + sl.hh) * D + c * 8), m);
@@ -228,7 +228,10 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
         }
     }
 
-    // ---- 4. Q codes, then K codes, from registers (8 bytes per row)
+    // ---- 4. Q codes, then K codes, from registers (8 bytes per row).  Q's
+    // scale bounds every Q element of its group, and K's every live K row, so
+    // only K rows at or past `used` (padding) can saturate -- or any row when
+    // the caller supplied the K amax (unfused).
     const size_t hD = (size_t)a.h * D;
     // global row t of this rank goes to out_base + t * hD within a section
     uint8_t *out_base = chunk + ((size_t)sl.b * L - row0) * hD + (size_t)j * D + c * 8;
@@ -240,11 +243,12 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
             if (valid(t)) {
                 float f[8];
                 to_f32x8<DT>(qv[i], f);
-                *reinterpret_cast<uint2 *>(out_base + (size_t)t * hD + a.lay.q) = int8_codes8(f, qsc);
+                *reinterpret_cast<uint2 *>(out_base + (size_t)t * hD + a.lay.q) = int8_codes8<false>(f, qsc);
             }
         }
     }
     to_f32x8<DT>(*reinterpret_cast<const uint4 *>(a.k_mean + ((size_t)sl.b * a.H + sl.hh) * D + c * 8), m);
+    const bool k_sat = !a.fused || g * kGQ + kGQ > a.used;   // CTA-uniform
 #pragma unroll
     for (int hk = 0; hk < 2; ++hk) {
         const Int8Scale ksc = sm.scl[1 + hk];
@@ -257,18 +261,18 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
 #pragma unroll
                 for (int x = 0; x < 8; x += 2)
                     f2unpack(f2sub(f2pack(f[x], f[x + 1]), f2pack(m[x], m[x + 1])), f[x], f[x + 1]);
-                *reinterpret_cast<uint2 *>(out_base + (size_t)t * hD + a.lay.k) = int8_codes8(f, ksc);
+                *reinterpret_cast<uint2 *>(out_base + (size_t)t * hD + a.lay.k) =
+                    k_sat ? int8_codes8<true>(f, ksc) : int8_codes8<false>(f, ksc);
             }
         }
     }
 
     // ---- 5. V codes from shared memory (rows this thread copied itself)
-    float vs[8], vl[8], vh[8];
+    float vs[8], vr[8];
 #pragma unroll
     for (int x = 0; x < 8; ++x) {
         vs[x] = sm.vs[c * 8 + x];
-        vl[x] = sm.vl[c * 8 + x];
-        vh[x] = sm.vh[c * 8 + x];
+        vr[x] = sm.vr[c * 8 + x];
     }
     cp_async_wait_all();
 #pragma unroll
@@ -277,7 +281,7 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
         if (valid(t)) {
             float f[8];
             to_f32x8<DT>(sm.vtile[(i * RL + rl) * NV + c], f);
-            *reinterpret_cast<uint2 *>(out_base + (size_t)t * hD + a.lay.v) = e4m3_codes8(f, vs, vl, vh);
+            *reinterpret_cast<uint2 *>(out_base + (size_t)t * hD + a.lay.v) = e4m3_codes8(f, vs, vr);
         }
     }
 }
