@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None, help="workload name (default: the headline one)")
     ap.add_argument("--mode", choices=["fused", "unfused"], default="fused")
+    ap.add_argument("--q-group", type=int, choices=[64, 128], default=128,
+                    help="Q group rows (64: Q groups are the K groups)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum CPU time spent on the oracle baseline sample")
@@ -178,16 +180,18 @@ def oracle_sample(wl):
         a = O.k_grouped_amax(k[0], inp.k_mean, swl.dtype, rank=0, world_size=P,
                              used_sequence=swl.used_sequence)
         mm, qb = zip(*[O.boundary_minmax(k[r], q[r], swl.dtype, rank=r, world_size=P,
-                                         used_sequence=swl.used_sequence) for r in range(P)])
+                                         used_sequence=swl.used_sequence, q_group=swl.q_group)
+                       for r in range(P)])
         g = np.ascontiguousarray(np.stack(mm))
         gq = np.ascontiguousarray(np.stack(qb))
         O.derive_k_boundary_amax(a, g, inp.k_mean, swl.dtype, rank=0, local_sequence=L,
                                  world_size=P)
         send = O.pack(q[0], k[0], v[0], inp.k_mean, swl.dtype, a, gq, inp.v_scale, rank=0,
-                      world_size=P)
+                      world_size=P, q_group=swl.q_group)
         recv0 = np.ascontiguousarray(np.broadcast_to(send[0], send.shape))
         O.unpack_for_sage(recv0, batch_size=swl.B, local_sequence=L, local_heads=1,
-                          head_dim=swl.D, world_size=P, scale_sequence=swl.scale_sequence)
+                          head_dim=swl.D, world_size=P, scale_sequence=swl.scale_sequence,
+                          q_group=swl.q_group)
 
     return run, metrics.step_bytes(swl) / P, swl
 
@@ -261,8 +265,8 @@ def run_ours(args, wl, rank, world, dist):
     km, vs = km_h.to(dev), vs_h.to(dev)
     path = UlyssesLowpPath(B=wl.B, L=wl.L, H=wl.H, D=wl.D, world_size=wl.P, dtype=dt,
                            used_sequence=wl.used_sequence, scale_sequence=wl.scale_sequence,
-                           aligned=wl.aligned, fused=(args.mode == "fused"), fold_exchange=True,
-                           device=dev)
+                           aligned=wl.aligned, q_group=wl.q_group, fused=(args.mode == "fused"),
+                           fold_exchange=True, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def barrier():
@@ -406,6 +410,8 @@ def main():
     args = parse()
     from quantize_pack_gb300 import configs
     wl = configs.BY_NAME[args.workload] if args.workload else configs.HEADLINE
+    if args.q_group != wl.q_group:
+        wl = wl.replace(q_group=args.q_group, name=f"{wl.name}_gq{args.q_group}")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     dist = None

@@ -54,8 +54,14 @@
  *    tensor is the stack of all ranks' tensors along a new leading axis of
  *    size world_size (written [P, ...] below).
  *
- * Geometry (K groups of 64 rows, Q groups of 128 rows, both on the global row
- * grid): first_G(r) = (r*L)/G, last_G(r) = ((r+1)*L-1)/G; slot j of rank r is
+ *  - q_group is the Q group width G_Q in rows: 128 (the default width of this
+ *    library; with aligned = 1, i.e. L % 128 == 0, no Q group crosses a rank)
+ *    or 64 (the variant whose Q groups are the K groups, one scale width for
+ *    both).  The pages print no Q width.  Every call that takes q_group must
+ *    get the same value along one path; other values give ULP_EINVAL.
+ *
+ * Geometry (K groups of 64 rows, Q groups of q_group rows, both on the global
+ * row grid): first_G(r) = (r*L)/G, last_G(r) = ((r+1)*L-1)/G; slot j of rank r is
  * global group first_G(r)+j; slots(L, G) = ceil(L/G) + (L % G != 0) bounds
  * the groups any rank touches.  Slots past the groups a rank touches hold
  * the floor value 1e-7 (amax) / rn(1e-7/127) (scale).
@@ -63,7 +69,7 @@
  * Chunk layout (one source rank -> one destination), each section 16-byte
  * aligned, in this order:
  *   Q int8 [B, L, h, D] | K int8 [B, L, h, D] | V e4m3 [B, L, h, D] |
- *   q_scale f32 [B, h, slots(L,128)] | k_scale f32 [B, h, slots(L,64)]
+ *   q_scale f32 [B, h, slots(L,q_group)] | k_scale f32 [B, h, slots(L,64)]
  * Chunk p of a source carries global heads [p*h, (p+1)*h).
  */
 #ifndef ULP_H
@@ -95,24 +101,25 @@ enum {
 
 #define ULP_ALL_RANKS (-1)
 
-/* slots(L, G): per-rank slot count for groups of G rows (G = 64 for K, 128 for
- * Q): ceil(L/G) + (L % G != 0).  Page "k_grouped_amax" (Returns:
+/* slots(L, G): per-rank slot count for groups of G rows (G = 64 for K, q_group
+ * for Q): ceil(L/G) + (L % G != 0).  Page "k_grouped_amax" (Returns:
  * [B, H, slots(L, 64)]) names it without printing it; this is the plainest
  * bound in (L, G) alone.  Returns -1 (ULP_EINVAL) for L < 1 or G < 1. */
 int ulp_slots(int local_sequence, int group);
 
 /* scale_widths(n) of page "unpack_for_sage" (scale_sequence paragraph):
- * consumer scale widths for n rows, *q_width = ceil(n/128),
- * *k_width = ceil(n/64).  ULP_EINVAL for n < 1 or NULL outputs. */
-int ulp_scale_widths(int n, int *q_width, int *k_width);
+ * consumer scale widths for n rows, *q_width = ceil(n/q_group),
+ * *k_width = ceil(n/64).  ULP_EINVAL for n < 1, a bad q_group or NULL
+ * outputs. */
+int ulp_scale_widths(int n, int q_group, int *q_width, int *k_width);
 
 /* Bytes of one chunk (layout above) for batch B, shard length L, h heads per
  * destination, head dim D.  ULP_EINVAL for non-positive sizes. */
-int ulp_chunk_bytes(int B, int L, int h, int D, size_t *chunk_bytes);
+int ulp_chunk_bytes(int B, int L, int h, int D, int q_group, size_t *chunk_bytes);
 
 /* Byte offsets of the five chunk sections: offsets[0..4] = Q, K, V,
  * q_scale, k_scale. */
-int ulp_chunk_offsets(int B, int L, int h, int D, size_t offsets[5]);
+int ulp_chunk_offsets(int B, int L, int h, int D, int q_group, size_t offsets[5]);
 
 /* Bytes of the workspace ulp_k_mean_global needs: 8 * P * B * ceil(L/512) * H * D. */
 int ulp_k_mean_workspace_bytes(int B, int L, int H, int D, int world_size, size_t *bytes);
@@ -182,14 +189,14 @@ int ulp_k_grouped_amax(const void *k, const void *k_mean, int dtype, int B, int 
  *   rank touching one group writes it under both e.
  * Also the Q boundary partials (input of ulp_pack):
  *   q_partial[b,H,e] = max(1e-7, max |f32(q[b,t,H,d])|) over the rank's rows
- *   of its first (e = 0) / last (e = 1) touched 128-row Q group.
+ *   of its first (e = 0) / last (e = 1) touched q_group-row Q group.
  *   k, q       [B, L, H, D] dtype  ([P, ...] for ULP_ALL_RANKS)
  *   minmax     [B, H, 2, 2, D] fp32 ([P, B, H, 2, 2, D] = the gathered buffer
  *              in group-rank order, for ULP_ALL_RANKS)
  *   q_partial  [B, H, 2] fp32 ([P, B, H, 2] for ULP_ALL_RANKS) */
 int ulp_boundary_minmax(const void *k, const void *q, int dtype, int B, int L, int H, int D,
-                        int rank, int world_size, int used_sequence, float *minmax,
-                        float *q_partial, ulp_stream_t stream);
+                        int rank, int world_size, int used_sequence, int q_group,
+                        float *minmax, float *q_partial, ulp_stream_t stream);
 
 /* derive_k_boundary_amax -- page "flashinfer.comm._ulysses_lowp.derive_k_boundary_amax".
  * Overwrites, in place, rank r's boundary slots (its first and last touched K
@@ -205,7 +212,7 @@ int ulp_derive_k_boundary_amax(float *grouped_amax, const float *gathered_minmax
                                int local_sequence, int world_size, ulp_stream_t stream);
 
 /* Sender pack of rank r into its P chunks (layout above).
- *   Q amax of 128-row group g: max(1e-7, max |f32(q)|) over g's rows; for the
+ *   Q amax of q_group-row group g: max(1e-7, max |f32(q)|) over g's rows; for the
  *   rank's first/last touched Q group it is the max of gathered_q_partial over
  *   the ranks touching g, otherwise computed from the rank's own rows.
  *   K amax: k_amax slots.  fused = 0: every slot is read from k_amax (the
@@ -230,8 +237,8 @@ int ulp_derive_k_boundary_amax(float *grouped_amax, const float *gathered_minmax
  *                       written at [p][r] (the exchange folded into the stores). */
 int ulp_pack(const void *q, const void *k, const void *v, const void *k_mean, int dtype,
              float *k_amax, const float *gathered_q_partial, const float *v_scale, int B, int L,
-             int H, int D, int rank, int world_size, int used_sequence, int fused, uint8_t *send,
-             int send_layout, int enable_pdl, ulp_stream_t stream);
+             int H, int D, int rank, int world_size, int used_sequence, int q_group, int fused,
+             uint8_t *send, int send_layout, int enable_pdl, ulp_stream_t stream);
 
 /* The all-to-all, emulated on one GPU: recv[p][s] = send[s][p] for the
  * [P, P, chunk_bytes] buffers of all ranks (page "unpack_for_sage": recv_u8 is
@@ -252,9 +259,9 @@ int ulp_alltoall_emulate(const uint8_t *send, uint8_t *recv, int world_size, siz
  * recv is [num_dests, P, chunk_bytes] and every output gains a leading
  * num_dests axis (num_dests = 1 is the single-destination call). */
 int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int D, int world_size,
-                        int aligned, int scale_sequence, int8_t *q8, int8_t *k8, uint8_t *v8,
-                        float *q_scale, float *k_scale, int num_dests, int enable_pdl,
-                        ulp_stream_t stream);
+                        int aligned, int scale_sequence, int q_group, int8_t *q8, int8_t *k8,
+                        uint8_t *v8, float *q_scale, float *k_scale, int num_dests,
+                        int enable_pdl, ulp_stream_t stream);
 
 /* Message of the calling thread's last failed call ("" if none). */
 const char *ulp_last_error(void);

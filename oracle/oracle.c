@@ -19,8 +19,9 @@
  *
  * Notation: P ranks, rank r owns global rows [r*L, (r+1)*L), S = P*L,
  * h = H/P heads per destination.  A global K group g is rows [64g, 64g+64),
- * a global Q group is rows [128g, 128g+128).  A rank's slot j of width G is
- * global group first_G(r) + j, first_G(r) = (r*L)/G.
+ * a global Q group is rows [gq*g, gq*g+gq), gq = 128 (default) or 64.  A
+ * rank's slot j of width G is global group first_G(r) + j,
+ * first_G(r) = (r*L)/G.
  *
  * Parity status: every function here is pinned by the tests under tests/
  * (test_oracle_*.py); the chunk byte layout, the axis order of the gathered
@@ -37,7 +38,9 @@
 #include "oracle.h"
 
 #define GK 64  /* K group rows (k_grouped_amax: "slots(L,64)") */
-#define GQ 128 /* Q group rows (reading: aligned=True <=> L % 128 == 0 keeps Q groups on one rank) */
+/* Q group rows gq are an argument: 128 by default (reading: aligned=True <=>
+ * L % 128 == 0 keeps Q groups on one rank), or 64, the variant whose Q groups
+ * are the K groups (one scale width for both). */
 
 /* The 1e-7 floor, as the binary32 value nearest to 1e-7. */
 static const float EPS = 1e-7f;
@@ -162,27 +165,27 @@ static size_t a16(size_t x) { return (x + 15) & ~(size_t)15; }
 
 /* Chunk (one source rank -> one destination rank) byte layout, in order:
  *   Q int8 [B, L, h, D] | K int8 [B, L, h, D] | V e4m3 [B, L, h, D] |
- *   q_scale f32 [B, h, slots(L,128)] | k_scale f32 [B, h, slots(L,64)]
+ *   q_scale f32 [B, h, slots(L,gq)] | k_scale f32 [B, h, slots(L,64)]
  * each section starting on a 16-byte boundary (a reading of this library:
  * the pages say only that recv_u8 is source-major [world_size, chunk_bytes]).
  * The alignment padding between sections is zero. */
-void orc_chunk_layout(int B, int L, int h, int D, size_t *off_q, size_t *off_k, size_t *off_v,
-                      size_t *off_qs, size_t *off_ks, size_t *chunk_bytes)
+void orc_chunk_layout(int B, int L, int h, int D, int gq, size_t *off_q, size_t *off_k,
+                      size_t *off_v, size_t *off_qs, size_t *off_ks, size_t *chunk_bytes)
 {
     size_t n = (size_t)B * L * h * D;
     *off_q = 0;
     *off_k = a16(n);
     *off_v = *off_k + a16(n);
     *off_qs = *off_v + a16(n);
-    *off_ks = *off_qs + a16(sizeof(float) * (size_t)B * h * orc_slots(L, GQ));
+    *off_ks = *off_qs + a16(sizeof(float) * (size_t)B * h * orc_slots(L, gq));
     *chunk_bytes = *off_ks + a16(sizeof(float) * (size_t)B * h * orc_slots(L, GK));
 }
 
 /* scale_widths(n): consumer scale-tensor widths for a sequence of n rows:
- * ceil(n/128) Q slots and ceil(n/64) K slots. */
-void orc_scale_widths(int n, int *q_width, int *k_width)
+ * ceil(n/gq) Q slots and ceil(n/64) K slots. */
+void orc_scale_widths(int n, int gq, int *q_width, int *k_width)
 {
-    *q_width = (n + GQ - 1) / GQ;
+    *q_width = (n + gq - 1) / gq;
     *k_width = (n + GK - 1) / GK;
 }
 
@@ -316,11 +319,12 @@ void orc_k_grouped_amax(const uint16_t *k, const uint16_t *k_mean, int dtype, in
  * statistic (0 = min, 1 = max); only live rows t < used count; a rank that
  * touches one group writes it under both e; -0 is stored as +0.
  * Also the Q boundary partial amax qb[b, H, e] = max(1e-7, max |f32(Q)|) over
- * the rank's rows of its first (e=0) / last (e=1) 128-row Q group (raw Q, so
+ * the rank's rows of its first (e=0) / last (e=1) gq-row Q group (raw Q, so
  * zero padding rows cannot raise it and used is not needed).
  * minmax: [B, H, 2, 2, D] for this rank; qb: [B, H, 2]. */
 void orc_boundary_minmax(const uint16_t *k, const uint16_t *q, int dtype, int B, int L, int H,
-                         int D, int rank, int world_size, int used, float *minmax, float *qb)
+                         int D, int rank, int world_size, int used, int gq, float *minmax,
+                         float *qb)
 {
     const int S = world_size * L;
     const int live = used >= 0 ? used : S;
@@ -344,9 +348,9 @@ void orc_boundary_minmax(const uint16_t *k, const uint16_t *q, int dtype, int B,
                     minmax[base + d] = mn;
                     minmax[base + D + d] = mx;
                 }
-                int gq = e == 0 ? first_group(rank, L, GQ) : last_group(rank, L, GQ);
-                int qlo = gq * GQ > row0 ? gq * GQ : row0;
-                int qhi = gq * GQ + GQ < row0 + L ? gq * GQ + GQ : row0 + L;
+                int g_q = e == 0 ? first_group(rank, L, gq) : last_group(rank, L, gq);
+                int qlo = g_q * gq > row0 ? g_q * gq : row0;
+                int qhi = g_q * gq + gq < row0 + L ? g_q * gq + gq : row0 + L;
                 float acc = -INFINITY;
                 for (int t = qlo; t < qhi; ++t)
                     for (int d = 0; d < D; ++d)
@@ -397,7 +401,7 @@ void orc_derive_k_boundary_amax(float *grouped_amax, const float *gathered, cons
 /* ------------------------------------------------------------------ pack */
 
 /* Sender pack of rank r (not printed on the pages; readings of this library):
- *  - Q amax of a 128-row global group g: max(1e-7, max |f32(Q)|) over all of
+ *  - Q amax of a gq-row global group g: max(1e-7, max |f32(Q)|) over all of
  *    g's rows, whichever ranks hold them.  A group inside rank r takes it from
  *    r's own rows; a boundary group (first/last touched) takes the max of the
  *    gathered partials qb of every rank touching g.  Slots past the touched
@@ -413,15 +417,15 @@ void orc_derive_k_boundary_amax(float *grouped_amax, const float *gathered, cons
  * zero-filled here first so the alignment padding of every chunk is zero. */
 void orc_pack(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *k_mean,
               int dtype, const float *k_amax, const float *gathered_qb, const float *v_scale,
-              int B, int L, int H, int D, int rank, int world_size, uint8_t *send)
+              int B, int L, int H, int D, int rank, int world_size, int gq, uint8_t *send)
 {
     const int P = world_size, S = P * L, h = H / P;
     const int row0 = rank * L;
-    const int nq = orc_slots(L, GQ), nk = orc_slots(L, GK);
-    const int fq = first_group(rank, L, GQ), lq = last_group(rank, L, GQ);
+    const int nq = orc_slots(L, gq), nk = orc_slots(L, GK);
+    const int fq = first_group(rank, L, gq), lq = last_group(rank, L, gq);
     const int fk = first_group(rank, L, GK);
     size_t oq, ok, ov, oqs, oks, cb;
-    orc_chunk_layout(B, L, h, D, &oq, &ok, &ov, &oqs, &oks, &cb);
+    orc_chunk_layout(B, L, h, D, gq, &oq, &ok, &ov, &oqs, &oks, &cb);
     memset(send, 0, (size_t)P * cb);
 
     float *qs = malloc(sizeof(float) * (size_t)nq);   /* per-slot scales of one (b, H) */
@@ -436,15 +440,15 @@ void orc_pack(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uin
                 if (g > lq) {
                     amax = EPS;
                 } else if (g == fq || g == lq) {
-                    int row_end = g * GQ + GQ < S ? g * GQ + GQ : S;
+                    int row_end = g * gq + gq < S ? g * gq + gq : S;
                     amax = -INFINITY;
-                    for (int rr = (g * GQ) / L; rr <= (row_end - 1) / L; ++rr) {
-                        int ee = g == first_group(rr, L, GQ) ? 0 : 1;
+                    for (int rr = (g * gq) / L; rr <= (row_end - 1) / L; ++rr) {
+                        int ee = g == first_group(rr, L, gq) ? 0 : 1;
                         amax = maxf(amax, gathered_qb[(((size_t)rr * B + b) * H + hh) * 2 + ee]);
                     }
                 } else {
                     float acc = -INFINITY;
-                    for (int t = g * GQ; t < g * GQ + GQ; ++t)
+                    for (int t = g * gq; t < g * gq + gq; ++t)
                         for (int d = 0; d < D; ++d)
                             acc = maxf(acc, fabsf(in_f32(q, (((size_t)b * L + (t - row0)) * H + hh) * D + d, dtype)));
                     amax = floor_eps(acc);
@@ -460,7 +464,7 @@ void orc_pack(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uin
             }
             for (int tl = 0; tl < L; ++tl) {
                 int t = row0 + tl;
-                float sq = qs[t / GQ - fq], sk = ks[t / GK - fk];
+                float sq = qs[t / gq - fq], sk = ks[t / GK - fk];
                 for (int d = 0; d < D; ++d) {
                     size_t src = (((size_t)b * L + tl) * H + hh) * D + d;
                     size_t dst = (((size_t)b * L + tl) * h + j) * D + d;
@@ -501,13 +505,13 @@ void orc_alltoall(const uint8_t *send, uint8_t *recv, int world_size, size_t chu
  *   source holding the group's first row, s = (G*g)/L, at its slot
  *   g - first_G(s) (reading: the other toucher carries the same bytes). */
 void orc_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int D, int world_size,
-                         int scale_sequence, int8_t *q8, int8_t *k8, uint8_t *v8, float *q_scale,
-                         float *k_scale)
+                         int scale_sequence, int gq, int8_t *q8, int8_t *k8, uint8_t *v8,
+                         float *q_scale, float *k_scale)
 {
     const int P = world_size, S = P * L, Spad = (S + 63) / 64 * 64;
-    const int nq = orc_slots(L, GQ), nk = orc_slots(L, GK);
+    const int nq = orc_slots(L, gq), nk = orc_slots(L, GK);
     size_t oq, ok, ov, oqs, oks, cb;
-    orc_chunk_layout(B, L, h, D, &oq, &ok, &ov, &oqs, &oks, &cb);
+    orc_chunk_layout(B, L, h, D, gq, &oq, &ok, &ov, &oqs, &oks, &cb);
     for (int b = 0; b < B; ++b)
         for (int t = 0; t < Spad; ++t)
             for (int j = 0; j < h; ++j)
@@ -526,13 +530,13 @@ void orc_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int D, int wo
                     v8[vdst] = chunk[ov + src];
                 }
     int wq, wk;
-    orc_scale_widths(scale_sequence >= 0 ? scale_sequence : S, &wq, &wk);
+    orc_scale_widths(scale_sequence >= 0 ? scale_sequence : S, gq, &wq, &wk);
     for (int b = 0; b < B; ++b)
         for (int j = 0; j < h; ++j) {
             for (int g = 0; g < wq; ++g) {
-                int s = (g * GQ) / L;
+                int s = (g * gq) / L;
                 const float *src = (const float *)(recv + (size_t)s * cb + oqs);
-                q_scale[((size_t)b * h + j) * wq + g] = src[((size_t)b * h + j) * nq + (g - first_group(s, L, GQ))];
+                q_scale[((size_t)b * h + j) * wq + g] = src[((size_t)b * h + j) * nq + (g - first_group(s, L, gq))];
             }
             for (int g = 0; g < wk; ++g) {
                 int s = (g * GK) / L;

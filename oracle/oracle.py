@@ -20,7 +20,7 @@ SOURCES = [os.path.join(HERE, "oracle.c")]
 HEADERS = [os.path.join(HERE, "oracle.h")]
 
 GK = 64
-GQ = 128
+GQ = 128       # default Q group rows; 64 selects the variant whose Q groups are the K groups
 
 _lib = None
 
@@ -97,23 +97,23 @@ def _declare(L):
     L.orc_slots.restype = _I
     L.orc_slots.argtypes = [_I, _I]
     L.orc_chunk_layout.restype = None
-    L.orc_chunk_layout.argtypes = [_I, _I, _I, _I] + [ctypes.POINTER(_SZ)] * 6
+    L.orc_chunk_layout.argtypes = [_I, _I, _I, _I, _I] + [ctypes.POINTER(_SZ)] * 6
     L.orc_scale_widths.restype = None
-    L.orc_scale_widths.argtypes = [_I, ctypes.POINTER(_I), ctypes.POINTER(_I)]
+    L.orc_scale_widths.argtypes = [_I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]
     L.orc_k_mean_global.restype = None
     L.orc_k_mean_global.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P]
     L.orc_k_grouped_amax.restype = None
     L.orc_k_grouped_amax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]
     L.orc_boundary_minmax.restype = None
-    L.orc_boundary_minmax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P]
+    L.orc_boundary_minmax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P]
     L.orc_derive_k_boundary_amax.restype = None
     L.orc_derive_k_boundary_amax.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I]
     L.orc_pack.restype = None
-    L.orc_pack.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]
+    L.orc_pack.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]
     L.orc_alltoall.restype = None
     L.orc_alltoall.argtypes = [_P, _P, _I, _SZ]
     L.orc_unpack_for_sage.restype = None
-    L.orc_unpack_for_sage.argtypes = [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]
+    L.orc_unpack_for_sage.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]
 
 
 def _ptr(a: np.ndarray, dtype) -> int:
@@ -154,16 +154,16 @@ def slots(L: int, G: int) -> int:
     return lib().orc_slots(L, G)
 
 
-def chunk_layout(B: int, L: int, h: int, D: int) -> dict:
+def chunk_layout(B: int, L: int, h: int, D: int, q_group: int = GQ) -> dict:
     v = [_SZ() for _ in range(6)]
-    lib().orc_chunk_layout(B, L, h, D, *[ctypes.byref(x) for x in v])
+    lib().orc_chunk_layout(B, L, h, D, q_group, *[ctypes.byref(x) for x in v])
     keys = ["q", "k", "v", "q_scale", "k_scale", "chunk_bytes"]
     return {k: int(x.value) for k, x in zip(keys, v)}
 
 
-def scale_widths(n: int) -> tuple:
+def scale_widths(n: int, q_group: int = GQ) -> tuple:
     q, k = _I(), _I()
-    lib().orc_scale_widths(n, ctypes.byref(q), ctypes.byref(k))
+    lib().orc_scale_widths(n, q_group, ctypes.byref(q), ctypes.byref(k))
     return q.value, k.value
 
 
@@ -187,13 +187,13 @@ def k_grouped_amax(k, k_mean, dtype, *, rank, world_size, used_sequence=None):
     return out
 
 
-def boundary_minmax(k, q, dtype, *, rank, world_size, used_sequence=None):
+def boundary_minmax(k, q, dtype, *, rank, world_size, used_sequence=None, q_group=GQ):
     """-> (minmax float32 [B, H, 2, 2, D], qb float32 [B, H, 2]) of one rank."""
     B, L, H, D = k.shape
     mm = np.empty((B, H, 2, 2, D), np.float32)
     qb = np.empty((B, H, 2), np.float32)
     lib().orc_boundary_minmax(_ptr(k, np.uint16), _ptr(q, np.uint16), dtype, B, L, H, D, rank,
-                              world_size, _opt(used_sequence), _ptr(mm, np.float32),
+                              world_size, _opt(used_sequence), q_group, _ptr(mm, np.float32),
                               _ptr(qb, np.float32))
     return mm, qb
 
@@ -210,16 +210,16 @@ def derive_k_boundary_amax(grouped_amax, gathered_minmax, k_mean, dtype, *, rank
     return grouped_amax
 
 
-def pack(q, k, v, k_mean, dtype, k_amax, gathered_qb, v_scale, *, rank, world_size):
+def pack(q, k, v, k_mean, dtype, k_amax, gathered_qb, v_scale, *, rank, world_size, q_group=GQ):
     """One rank's send buffer uint8 [P, chunk_bytes]."""
     B, L, H, D = q.shape
     h = H // world_size
-    cb = chunk_layout(B, L, h, D)["chunk_bytes"]
+    cb = chunk_layout(B, L, h, D, q_group)["chunk_bytes"]
     send = np.zeros((world_size, cb), np.uint8)
     lib().orc_pack(_ptr(q, np.uint16), _ptr(k, np.uint16), _ptr(v, np.uint16),
                    _ptr(k_mean, np.uint16), dtype, _ptr(k_amax, np.float32),
                    _ptr(gathered_qb, np.float32), _ptr(v_scale, np.float32), B, L, H, D, rank,
-                   world_size, _ptr(send, np.uint8))
+                   world_size, q_group, _ptr(send, np.uint8))
     return send
 
 
@@ -232,17 +232,17 @@ def alltoall(send_all):
 
 
 def unpack_for_sage(recv_u8, *, batch_size, local_sequence, local_heads, head_dim, world_size,
-                    scale_sequence=None):
+                    scale_sequence=None, q_group=GQ):
     B, L, h, D, P = batch_size, local_sequence, local_heads, head_dim, world_size
     S = P * L
     Spad = (S + 63) // 64 * 64
-    wq, wk = scale_widths(S if scale_sequence is None else scale_sequence)
+    wq, wk = scale_widths(S if scale_sequence is None else scale_sequence, q_group)
     q8 = np.empty((B, S, h, D), np.int8)
     k8 = np.empty((B, S, h, D), np.int8)
     v8 = np.empty((B, D, h, Spad), np.uint8)
     qs = np.empty((B, h, wq), np.float32)
     ks = np.empty((B, h, wk), np.float32)
-    lib().orc_unpack_for_sage(_ptr(recv_u8, np.uint8), B, L, h, D, P, _opt(scale_sequence),
+    lib().orc_unpack_for_sage(_ptr(recv_u8, np.uint8), B, L, h, D, P, _opt(scale_sequence), q_group,
                               _ptr(q8, np.int8), _ptr(k8, np.int8), _ptr(v8, np.uint8),
                               _ptr(qs, np.float32), _ptr(ks, np.float32))
     return q8, k8, v8, qs, ks
@@ -251,7 +251,7 @@ def unpack_for_sage(recv_u8, *, batch_size, local_sequence, local_heads, head_di
 # -------------------------------------------------- the whole emulated path
 
 def forward(q_sh, k_sh, v_sh, k_mean, v_scale, dtype, *, used_sequence=None,
-            scale_sequence=None, ranks=None, dests=None):
+            scale_sequence=None, ranks=None, dests=None, q_group=GQ):
     """Every step of the path for an emulated Ulysses group of P ranks.
 
     q_sh, k_sh, v_sh: uint16 [P, B, L, H, D] shards.  Returns a dict with the
@@ -265,7 +265,8 @@ def forward(q_sh, k_sh, v_sh, k_mean, v_scale, dtype, *, used_sequence=None,
     ga0 = np.stack([k_grouped_amax(k_sh[r], k_mean, dtype, rank=r, world_size=P,
                                    used_sequence=used_sequence) for r in range(P)])
     mm, qb = zip(*[boundary_minmax(k_sh[r], q_sh[r], dtype, rank=r, world_size=P,
-                                   used_sequence=used_sequence) for r in range(P)])
+                                   used_sequence=used_sequence, q_group=q_group)
+                   for r in range(P)])
     gathered = np.ascontiguousarray(np.stack(mm))
     gathered_qb = np.ascontiguousarray(np.stack(qb))
     ga = ga0.copy()
@@ -273,12 +274,13 @@ def forward(q_sh, k_sh, v_sh, k_mean, v_scale, dtype, *, used_sequence=None,
         derive_k_boundary_amax(ga[r], gathered, k_mean, dtype, rank=r, local_sequence=L,
                                world_size=P)
     send = np.stack([pack(q_sh[r], k_sh[r], v_sh[r], k_mean, dtype, np.ascontiguousarray(ga[r]),
-                          gathered_qb, v_scale, rank=r, world_size=P) for r in range(P)])
+                          gathered_qb, v_scale, rank=r, world_size=P, q_group=q_group)
+                     for r in range(P)])
     recv = alltoall(send)
     outs = {}
     for p in (range(P) if dests is None else dests):
         outs[p] = unpack_for_sage(np.ascontiguousarray(recv[p]), batch_size=B, local_sequence=L,
                                   local_heads=h, head_dim=D, world_size=P,
-                                  scale_sequence=scale_sequence)
+                                  scale_sequence=scale_sequence, q_group=q_group)
     return {"amax_kernel": ga0, "minmax": gathered, "qb": gathered_qb, "amax": ga,
             "send": send, "recv": recv, "out": outs}

@@ -35,6 +35,8 @@ class Workload:
     # scale_sequence handed to unpack: None, or "used" (= used_sequence)
     scale_to_used: bool = False
     aligned: Optional[bool] = None
+    # Q group rows: 128, or 64 (the variant whose Q groups are the K groups)
+    q_group: int = 128
     # value recipe
     qv_dist: str = "normal"          # "normal" (N(0,1)) or "t3" (Student-t, nu=3)
     k_mean_std: float = 1.0          # std of the per-(head, channel) K mean
@@ -86,6 +88,7 @@ class Workload:
             "used_sequence": self.used_sequence,
             "scale_sequence": self.scale_sequence,
             "aligned": self.aligned,
+            "q_group": self.q_group,
         }
 
 

@@ -1,7 +1,7 @@
 // K grouped amax (page "k_grouped_amax"), the raw-K boundary min/max producer
 // and the boundary derive (page "derive_k_boundary_amax").
 //
-// All three are reductions over at most 64 (K) or 128 (Q) rows of one head.
+// All three are reductions over at most 64 (K) or q_group <= 128 (Q) rows of one head.
 // Threads own one 16-byte column vector (8 channels) and a row lane; loads are
 // 16-byte and coalesced along the head's D contiguous elements; the maxima are
 // fp32 fmaxf trees (exact, so order-independent).
@@ -83,6 +83,7 @@ struct MinmaxArgs {
     const uint16_t *k, *q;
     float *minmax, *qpart;
     int B, L, H, P, rank, used;
+    int gq;   // Q group rows, 64 or 128
 };
 
 // One CTA per (rank, b, head, e): e = 0 first touched group, e = 1 last.
@@ -140,19 +141,20 @@ __global__ void __launch_bounds__(128) boundary_minmax_kernel(MinmaxArgs a)
     }
 
     // ---- Q: partial amax over the rank's rows of its first / last Q group
-    const int gq = e == 0 ? first_group(r, a.L, kGQ) : last_group(r, a.L, kGQ);
-    const int qlo = max(gq * kGQ, row0), qhi = min(gq * kGQ + kGQ, row0 + a.L);
+    // (ITQ covers the widest group; rows past a narrower group fail the test)
+    const int gq = e == 0 ? first_group(r, a.L, a.gq) : last_group(r, a.L, a.gq);
+    const int qlo = max(gq * a.gq, row0), qhi = min(gq * a.gq + a.gq, row0 + a.L);
     float qa = -INFINITY;
     {
         uint4 v[ITQ];
 #pragma unroll
         for (int i = 0; i < ITQ; ++i) {
-            const int t = gq * kGQ + i * RL + rl;
+            const int t = gq * a.gq + i * RL + rl;
             if (t >= qlo && t < qhi) v[i] = ld_stream(a.q + off + (size_t)(t - row0) * HD);
         }
 #pragma unroll
         for (int i = 0; i < ITQ; ++i) {
-            const int t = gq * kGQ + i * RL + rl;
+            const int t = gq * a.gq + i * RL + rl;
             if (t >= qlo && t < qhi) {
                 float f[8];
                 to_f32x8<DT>(v[i], f);
@@ -263,15 +265,16 @@ int ulp_k_grouped_amax(const void *k, const void *k_mean, int dtype, int B, int 
 }
 
 int ulp_boundary_minmax(const void *k, const void *q, int dtype, int B, int L, int H, int D,
-                        int rank, int world_size, int used_sequence, float *minmax,
-                        float *q_partial, ulp_stream_t stream)
+                        int rank, int world_size, int used_sequence, int q_group,
+                        float *minmax, float *q_partial, ulp_stream_t stream)
 {
     if (int s = check_common(dtype, B, L, H, D, rank, world_size, used_sequence, -1)) return s;
+    if (int s = check_q_group(q_group, "boundary_minmax")) return s;
     if (!aligned16(k) || !aligned16(q) || !aligned4(minmax) || !aligned4(q_partial))
         return fail(ULP_EALIGN, "boundary_minmax: k, q must be 16-byte aligned, minmax, q_partial 4-byte aligned");
     const int nranks = rank == ULP_ALL_RANKS ? world_size : 1;
     MinmaxArgs a{(const uint16_t *)k, (const uint16_t *)q, minmax, q_partial, B, L, H, world_size, rank,
-                 used_sequence < 0 ? L * world_size : used_sequence};
+                 used_sequence < 0 ? L * world_size : used_sequence, q_group};
     unsigned grid = 0;
     if (int s = grid_of((long long)nranks * B * H * 2, &grid, "boundary_minmax")) return s;
     ULP_DISPATCH(D, dtype, (launch_kernel(boundary_minmax_kernel<kD, kDT>, dim3(grid), dim3(128), (cudaStream_t)stream, false, a)));

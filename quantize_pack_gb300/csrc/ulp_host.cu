@@ -37,6 +37,13 @@ int check_world(int world_size)
     return ULP_OK;
 }
 
+int check_q_group(int q_group, const char *what)
+{
+    if (q_group != 64 && q_group != 128)
+        return fail(ULP_EINVAL, "%s: q_group must be 64 or 128 (got %d)", what, q_group);
+    return ULP_OK;
+}
+
 int check_common(int dtype, int B, int L, int H, int D, int rank, int world_size,
                  int used_sequence, int enable_pdl)
 {
@@ -92,19 +99,21 @@ int ulp_slots(int local_sequence, int group)
     return slots(local_sequence, group);
 }
 
-int ulp_scale_widths(int n, int *q_width, int *k_width)
+int ulp_scale_widths(int n, int q_group, int *q_width, int *k_width)
 {
     if (n < 1 || !q_width || !k_width) return fail(ULP_EINVAL, "scale_widths: n must be positive (%d)", n);
-    *q_width = (n + kGQ - 1) / kGQ;
+    if (int s = check_q_group(q_group, "scale_widths")) return s;
+    *q_width = (n + q_group - 1) / q_group;
     *k_width = (n + kGK - 1) / kGK;
     return ULP_OK;
 }
 
-int ulp_chunk_offsets(int B, int L, int h, int D, size_t offsets[5])
+int ulp_chunk_offsets(int B, int L, int h, int D, int q_group, size_t offsets[5])
 {
     if (B < 1 || L < 1 || h < 1 || D < 1 || !offsets)
         return fail(ULP_EINVAL, "chunk_offsets: sizes must be positive");
-    ChunkLayout c = chunk_layout(B, L, h, D);
+    if (int s = check_q_group(q_group, "chunk_offsets")) return s;
+    ChunkLayout c = chunk_layout(B, L, h, D, q_group);
     offsets[0] = c.q;
     offsets[1] = c.k;
     offsets[2] = c.v;
@@ -113,11 +122,12 @@ int ulp_chunk_offsets(int B, int L, int h, int D, size_t offsets[5])
     return ULP_OK;
 }
 
-int ulp_chunk_bytes(int B, int L, int h, int D, size_t *chunk_bytes)
+int ulp_chunk_bytes(int B, int L, int h, int D, int q_group, size_t *chunk_bytes)
 {
     if (B < 1 || L < 1 || h < 1 || D < 1 || !chunk_bytes)
         return fail(ULP_EINVAL, "chunk_bytes: sizes must be positive");
-    *chunk_bytes = chunk_layout(B, L, h, D).bytes;
+    if (int s = check_q_group(q_group, "chunk_bytes")) return s;
+    *chunk_bytes = chunk_layout(B, L, h, D, q_group).bytes;
     return ULP_OK;
 }
 

@@ -16,7 +16,7 @@
 namespace ulp {
 
 constexpr int kGK = 64;    // K group rows
-constexpr int kGQ = 128;   // Q group rows
+constexpr int kGQ = 128;   // default Q group rows (q_group = 64 is the other width)
 constexpr float kEps = 1e-7f;
 
 // ------------------------------------------------------------------ errors
@@ -41,7 +41,7 @@ struct ChunkLayout {
     size_t q, k, v, qs, ks, bytes;
 };
 
-__host__ __device__ __forceinline__ ChunkLayout chunk_layout(int B, int L, int h, int D)
+__host__ __device__ __forceinline__ ChunkLayout chunk_layout(int B, int L, int h, int D, int gq)
 {
     ChunkLayout c;
     size_t n = (size_t)B * L * h * D;
@@ -49,7 +49,7 @@ __host__ __device__ __forceinline__ ChunkLayout chunk_layout(int B, int L, int h
     c.k = align16(n);
     c.v = c.k + align16(n);
     c.qs = c.v + align16(n);
-    c.ks = c.qs + align16(sizeof(float) * (size_t)B * h * slots(L, kGQ));
+    c.ks = c.qs + align16(sizeof(float) * (size_t)B * h * slots(L, gq));
     c.bytes = c.ks + align16(sizeof(float) * (size_t)B * h * slots(L, kGK));
     return c;
 }
@@ -57,6 +57,7 @@ __host__ __device__ __forceinline__ ChunkLayout chunk_layout(int B, int L, int h
 // ---------------------------------------------------------- argument checks
 
 bool aligned16(const void *p);
+int check_q_group(int q_group, const char *what);
 bool aligned4(const void *p);
 int check_common(int dtype, int B, int L, int H, int D, int rank, int world_size,
                  int used_sequence, int enable_pdl);

@@ -3,10 +3,12 @@
 // all-to-all moves (page "unpack_for_sage": recv_u8 is the source-major
 // buffer of chunks; Returns: the V scale remains with the caller).
 //
-// Work unit: a "slab" = one 128-row global Q group of one head on one rank,
-// one CTA each.  Q and K rows are loaded once into registers, V rows into
-// shared memory; the Q amax and the amax of the slab's two 64-row K groups are
-// reduced in the CTA and the codes are written from the same registers.
+// Work unit: a "slab" = the rows of one 128-row global group of one head on
+// one rank, one CTA each.  Q and K rows are loaded once into registers, V rows
+// into shared memory; the Q amax (of the slab's one 128-row Q group, or of its
+// two 64-row Q groups when q_group = 64) and the amax of its two 64-row K
+// groups are reduced in the CTA and the codes are written from the same
+// registers.
 // Boundary groups (the rank's first/last touched group) take their amax from
 // the gathered partials (Q) or the derived slots (K), so every input byte
 // crosses HBM once.  Quotients use a correctly rounded reciprocal with an
@@ -23,39 +25,43 @@ struct PackArgs {
     const float *v_scale;  // [B, H, D]
     uint8_t *send;
     ChunkLayout lay;
-    int B, L, H, P, h, rank, used, fused, layout, nq, nk;
+    int B, L, H, P, h, rank, used, fused, layout, nq, nk;   // nq = slots(L, q_group)
     int early;   // read q, k, v, k_mean, v_scale before waiting for the preceding kernel
 };
 
 constexpr int kPackThreads = 512;
+constexpr int kSlab = 128;   // rows of a slab: one 128-row group = two 64-row groups
 
 template <int D>
 struct PackSmem {
-    uint4 vtile[kGQ * D / 8];                 // V rows of the slab
-    float red[kPackThreads / 32][3];          // per-warp Q, K0, K1 maxima
-    Int8Scale scl[3];                         // Q, K group 0, K group 1
+    uint4 vtile[kSlab * D / 8];               // V rows of the slab
+    float red[kPackThreads / 32][4];          // per-warp Q0, Q1, K0, K1 maxima
+    Int8Scale scl[4];                         // Q (first half), Q second half, K group 0, K group 1
     float vs[D], vr[D];                       // V channel scales and their reciprocals
 };
 
 struct Slab {
-    int rk, r, b, hh, jq, g, L, S, row0, tq, fk, lk, tk, gu;
+    int rk, r, b, hh, js, g, L, S, row0, ts, fk, lk, tk, gu;   // js, ts: slab slot, touched slabs
 };
 
 // One slab: FULL = all 128 rows belong to the rank and none is excluded from
-// the K amax (so no per-row predicate is needed).
-template <int D, int DT, bool FULL>
+// the K amax (so no per-row predicate is needed).  GQ = Q group rows: 128 (one
+// Q group per slab, slot js) or 64 (Q groups are the K groups 2g, 2g+1).
+template <int D, int DT, int GQ, bool FULL>
 __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, PackSmem<D> &sm)
 {
     constexpr int NV = D / 8;                 // 16-byte vectors per row
     constexpr int RL = kPackThreads / NV;     // row lanes
-    constexpr int IT = kGQ / RL;              // rows per thread
+    constexpr int IT = kSlab / RL;            // rows per thread
     constexpr int NW = kPackThreads / 32;
+    constexpr int NQH = kSlab / GQ;           // Q groups per slab
     static_assert(IT % 2 == 0 && RL * IT / 2 == kGK, "slab halves must be the K groups");
+    static_assert(GQ == 64 || GQ == 128, "Q groups of 64 or 128 rows");
 
     const int c = threadIdx.x % NV, rl = threadIdx.x / NV;
     const int L = sl.L, row0 = sl.row0, g = sl.g;
     const size_t HD = (size_t)a.H * D;
-    const int t_first = g * kGQ + rl;                 // row i is t_first + i * RL
+    const int t_first = g * kSlab + rl;               // row i is t_first + i * RL
     // global row t of this rank lives at in_base + t * HD
     const size_t in_base = ((size_t)sl.rk * a.B + sl.b) * L * HD - (size_t)row0 * HD + (size_t)sl.hh * D + c * 8;
     auto valid = [&](int t) { return FULL || (t >= row0 && t < row0 + L); };
@@ -87,17 +93,18 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
     float m[8];
     to_f32x8<DT>(*reinterpret_cast<const uint4 *>(a.k_mean + ((size_t)sl.b * a.H + sl.hh) * D + c * 8), m);
 
-    // ---- 3. amax: Q over all rows of the slab, K per 64-row half.  Per
-    // channel pair, a running max and min of the raw 16-bit values (exact);
-    // then max |Q| = max(maxQ, -minQ) and, rn subtraction being monotone,
-    // max |rn(K - m)| = max(rn(maxK - m), rn(m - minK)).
-    float qmax = -INFINITY, kmax0 = -INFINITY, kmax1 = -INFINITY;
-    {
+    // ---- 3. amax: Q per Q group of the slab (all rows, or each 64-row
+    // half), K per 64-row half.  Per channel pair, a running max and min of
+    // the raw 16-bit values (exact); then max |Q| = max(maxQ, -minQ) and, rn
+    // subtraction being monotone, max |rn(K - m)| = max(rn(maxK - m), rn(m - minK)).
+    float qmax0 = -INFINITY, qmax1 = -INFINITY, kmax0 = -INFINITY, kmax1 = -INFINITY;
+#pragma unroll
+    for (int hq = 0; hq < NQH; ++hq) {
         Pair16<DT> pr[4];
 #pragma unroll
         for (int x = 0; x < 4; ++x) pr[x].init();
 #pragma unroll
-        for (int i = 0; i < IT; ++i) {
+        for (int i = hq * IT / NQH; i < (hq + 1) * IT / NQH; ++i) {
             if (valid(t_first + i * RL)) {
                 pr[0].add(qv[i].x);
                 pr[1].add(qv[i].y);
@@ -105,11 +112,14 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
                 pr[3].add(qv[i].w);
             }
         }
+        float v = -INFINITY;
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
             const float2 hi = pair_f32<DT>(pr[x].mx), lo = pair_f32<DT>(pr[x].mn);
-            qmax = fmaxf(qmax, fmaxf(fmaxf(hi.x, -lo.x), fmaxf(hi.y, -lo.y)));
+            v = fmaxf(v, fmaxf(fmaxf(hi.x, -lo.x), fmaxf(hi.y, -lo.y)));
         }
+        if (hq == 0) qmax0 = v;
+        else qmax1 = v;
     }
 #pragma unroll
     for (int hk = 0; hk < 2; ++hk) {
@@ -139,39 +149,51 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (a.early) pdl_wait();          // k_amax, the partials and the chunks belong to the chain
-    qmax = warp_max(qmax);
+    qmax0 = warp_max(qmax0);
+    if (NQH == 2) qmax1 = warp_max(qmax1);
     kmax0 = warp_max(kmax0);
     kmax1 = warp_max(kmax1);
     if (lane == 0) {
-        sm.red[warp][0] = qmax;
-        sm.red[warp][1] = kmax0;
-        sm.red[warp][2] = kmax1;
+        sm.red[warp][0] = qmax0;
+        sm.red[warp][1] = qmax1;
+        sm.red[warp][2] = kmax0;
+        sm.red[warp][3] = kmax1;
     }
     __syncthreads();
 
     const size_t amax_row = (((size_t)sl.rk * a.B + sl.b) * a.H + sl.hh) * a.nk;
     if (warp == 0) {
-        qmax = lane < NW ? sm.red[lane][0] : -INFINITY;
-        kmax0 = lane < NW ? sm.red[lane][1] : -INFINITY;
-        kmax1 = lane < NW ? sm.red[lane][2] : -INFINITY;
-        qmax = warp_max(qmax);
+        qmax0 = lane < NW ? sm.red[lane][0] : -INFINITY;
+        qmax1 = lane < NW ? sm.red[lane][1] : -INFINITY;
+        kmax0 = lane < NW ? sm.red[lane][2] : -INFINITY;
+        kmax1 = lane < NW ? sm.red[lane][3] : -INFINITY;
+        qmax0 = warp_max(qmax0);
+        if (NQH == 2) qmax1 = warp_max(qmax1);
         kmax0 = warp_max(kmax0);
         kmax1 = warp_max(kmax1);
-        if (lane == 0) {
-            float qam;
-            if (sl.jq == 0 || sl.jq == sl.tq - 1) {         // boundary: merge the gathered partials
-                const int rend = min(g * kGQ + kGQ, sl.S);
-                qam = -INFINITY;
-                for (int rr = (g * kGQ) / L; rr <= (rend - 1) / L; ++rr) {
-                    const int ee = g == first_group(rr, L, kGQ) ? 0 : 1;
-                    qam = fmaxf(qam, a.qpart[(((size_t)rr * a.B + sl.b) * a.H + sl.hh) * 2 + ee]);
+        if (lane < NQH) {
+            // Q group gg of this lane; its slot range and boundary test
+            const int gg = NQH * g + lane;
+            const bool touched = NQH == 1 || (gg >= sl.fk && gg <= sl.lk);
+            const bool boundary = NQH == 1 ? (sl.js == 0 || sl.js == sl.ts - 1) : (gg == sl.fk || gg == sl.lk);
+            float qs = 1.0f;                                 // a half with no row of the rank
+            if (touched) {
+                float qam;
+                if (boundary) {                              // merge the gathered partials
+                    const int rend = min(gg * GQ + GQ, sl.S);
+                    qam = -INFINITY;
+                    for (int rr = (gg * GQ) / L; rr <= (rend - 1) / L; ++rr) {
+                        const int ee = gg == first_group(rr, L, GQ) ? 0 : 1;
+                        qam = fmaxf(qam, a.qpart[(((size_t)rr * a.B + sl.b) * a.H + sl.hh) * 2 + ee]);
+                    }
+                } else {
+                    qam = floor_eps(lane == 0 ? qmax0 : qmax1);
                 }
-            } else {
-                qam = floor_eps(qmax);
+                qs = __fdiv_rn(qam, 127.0f);
             }
-            sm.scl[0] = int8_scale(__fdiv_rn(qam, 127.0f));
-        } else if (lane == 1 || lane == 2) {
-            const int hk = lane - 1, gk = 2 * g + hk;
+            sm.scl[lane] = int8_scale(qs);
+        } else if (lane == 2 || lane == 3) {
+            const int hk = lane - 2, gk = 2 * g + hk;
             float ks = 1.0f;
             if (gk >= sl.fk && gk <= sl.lk) {
                 const int jk = gk - sl.fk;
@@ -184,7 +206,7 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
                 }
                 ks = __fdiv_rn(kam, 127.0f);
             }
-            sm.scl[1 + hk] = int8_scale(ks);
+            sm.scl[2 + hk] = int8_scale(ks);
         }
     }
     __syncthreads();
@@ -199,12 +221,16 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
         float *qs_out = reinterpret_cast<float *>(chunk + a.lay.qs) + ((size_t)sl.b * a.h + j) * a.nq;
         float *ks_out = reinterpret_cast<float *>(chunk + a.lay.ks) + ((size_t)sl.b * a.h + j) * a.nk;
         const int t = threadIdx.x;
-        if (t == 0) qs_out[sl.jq] = sm.scl[0].s;
-        if (t == 1 || t == 2) {
-            const int gk = 2 * g + (t - 1);
+        if (NQH == 1 && t == 0) qs_out[sl.js] = sm.scl[0].s;
+        if (NQH == 2 && t < 2) {
+            const int gg = 2 * g + t;
+            if (gg >= sl.fk && gg <= sl.lk) qs_out[gg - sl.fk] = sm.scl[t].s;
+        }
+        if (t == 2 || t == 3) {
+            const int gk = 2 * g + (t - 2);
             if (gk >= sl.fk && gk <= sl.lk) ks_out[gk - sl.fk] = sm.scl[t].s;
         }
-        if (sl.jq == sl.tq - 1) {                        // slots past the touched groups
+        if (sl.js == sl.ts - 1) {                        // slots past the touched groups
             if (sl.b == a.B - 1 && j == a.h - 1) {
                 // the last writer of the chunk's scale sections zeroes their
                 // alignment padding, so every chunk byte is defined
@@ -214,7 +240,8 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
                 if (nqs + t < (a.lay.ks - a.lay.qs) / 4) qsec[nqs + t] = 0.0f;
                 if (nks + t < (a.lay.bytes - a.lay.ks) / 4) ksec[nks + t] = 0.0f;
             }
-            if (sl.tq + t < a.nq) qs_out[sl.tq + t] = __fdiv_rn(kEps, 127.0f);
+            const int tq = NQH == 1 ? sl.ts : sl.tk;    // touched Q groups
+            if (tq + t < a.nq) qs_out[tq + t] = __fdiv_rn(kEps, 127.0f);
             if (sl.tk + t < a.nk) {
                 float kam;
                 if (a.fused) {
@@ -235,10 +262,11 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
     const size_t hD = (size_t)a.h * D;
     // global row t of this rank goes to out_base + t * hD within a section
     uint8_t *out_base = chunk + ((size_t)sl.b * L - row0) * hD + (size_t)j * D + c * 8;
-    {
-        const Int8Scale qsc = sm.scl[0];
 #pragma unroll
-        for (int i = 0; i < IT; ++i) {
+    for (int hq = 0; hq < NQH; ++hq) {
+        const Int8Scale qsc = sm.scl[hq];
+#pragma unroll
+        for (int i = hq * IT / NQH; i < (hq + 1) * IT / NQH; ++i) {
             const int t = t_first + i * RL;
             if (valid(t)) {
                 float f[8];
@@ -248,10 +276,10 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
         }
     }
     to_f32x8<DT>(*reinterpret_cast<const uint4 *>(a.k_mean + ((size_t)sl.b * a.H + sl.hh) * D + c * 8), m);
-    const bool k_sat = !a.fused || g * kGQ + kGQ > a.used;   // CTA-uniform
+    const bool k_sat = !a.fused || g * kSlab + kSlab > a.used;   // CTA-uniform
 #pragma unroll
     for (int hk = 0; hk < 2; ++hk) {
-        const Int8Scale ksc = sm.scl[1 + hk];
+        const Int8Scale ksc = sm.scl[2 + hk];
 #pragma unroll
         for (int i = hk * IT / 2; i < (hk + 1) * IT / 2; ++i) {
             const int t = t_first + i * RL;
@@ -295,35 +323,35 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
 //     then warp 0 merges the warps, applies the boundary rules and publishes
 //     the scales;
 //  4. Q/K codes from the registers; 5. V codes from shared memory.
-template <int D, int DT>
+template <int D, int DT, int GQ>
 __global__ void __launch_bounds__(kPackThreads, 2) pack_kernel(PackArgs a)
 {
     __shared__ __align__(16) PackSmem<D> sm;
     pdl_trigger();
     Slab sl;
     sl.hh = blockIdx.x;
-    sl.jq = blockIdx.y;
+    sl.js = blockIdx.y;
     sl.rk = blockIdx.z / a.B;
     sl.b = blockIdx.z - sl.rk * a.B;
     sl.r = a.rank >= 0 ? a.rank : sl.rk;
     sl.L = a.L;
     sl.S = a.P * a.L;
     sl.row0 = sl.r * a.L;
-    const int fq = first_group(sl.r, a.L, kGQ);
-    sl.tq = last_group(sl.r, a.L, kGQ) - fq + 1;
-    if (sl.jq >= sl.tq) {
+    const int fs = first_group(sl.r, a.L, kSlab);
+    sl.ts = last_group(sl.r, a.L, kSlab) - fs + 1;
+    if (sl.js >= sl.ts) {
         pdl_wait();
         return;
     }
-    sl.g = fq + sl.jq;
+    sl.g = fs + sl.js;
     sl.fk = first_group(sl.r, a.L, kGK);
     sl.lk = last_group(sl.r, a.L, kGK);
     sl.tk = sl.lk - sl.fk + 1;
     sl.gu = a.used < sl.S ? (a.used - 1) / kGK : -1;
-    const bool full = sl.g * kGQ >= sl.row0 && sl.g * kGQ + kGQ <= sl.row0 + a.L &&
+    const bool full = sl.g * kSlab >= sl.row0 && sl.g * kSlab + kSlab <= sl.row0 + a.L &&
                       !(sl.gu >= 0 && sl.gu / 2 == sl.g);
-    if (full) pack_slab<D, DT, true>(a, sl, sm);
-    else pack_slab<D, DT, false>(a, sl, sm);
+    if (full) pack_slab<D, DT, GQ, true>(a, sl, sm);
+    else pack_slab<D, DT, GQ, false>(a, sl, sm);
 }
 
 }  // namespace ulp
@@ -332,10 +360,12 @@ using namespace ulp;
 
 extern "C" int ulp_pack(const void *q, const void *k, const void *v, const void *k_mean, int dtype,
                         float *k_amax, const float *gathered_q_partial, const float *v_scale, int B,
-                        int L, int H, int D, int rank, int world_size, int used_sequence, int fused,
-                        uint8_t *send, int send_layout, int enable_pdl, ulp_stream_t stream)
+                        int L, int H, int D, int rank, int world_size, int used_sequence,
+                        int q_group, int fused, uint8_t *send, int send_layout, int enable_pdl,
+                        ulp_stream_t stream)
 {
     if (int s = check_common(dtype, B, L, H, D, rank, world_size, used_sequence, enable_pdl)) return s;
+    if (int s = check_q_group(q_group, "pack")) return s;
     if (fused != 0 && fused != 1) return fail(ULP_EINVAL, "pack: fused must be 0 or 1 (got %d)", fused);
     if (send_layout != ULP_SEND_SOURCE_MAJOR && send_layout != ULP_SEND_DEST_MAJOR)
         return fail(ULP_EINVAL, "pack: send_layout must be 0 or 1 (got %d)", send_layout);
@@ -345,26 +375,33 @@ extern "C" int ulp_pack(const void *q, const void *k, const void *v, const void 
                                 "k_amax and gathered_q_partial 4-byte aligned");
     const int h = H / world_size;
     PackArgs a{(const uint16_t *)q, (const uint16_t *)k, (const uint16_t *)v, (const uint16_t *)k_mean,
-               k_amax, gathered_q_partial, v_scale, send, chunk_layout(B, L, h, D),
+               k_amax, gathered_q_partial, v_scale, send, chunk_layout(B, L, h, D, q_group),
                B, L, H, world_size, h, rank,
                used_sequence < 0 ? L * world_size : used_sequence, fused, send_layout,
-               slots(L, kGQ), slots(L, kGK)};
+               slots(L, q_group), slots(L, kGK)};
     // A shard touches at least ceil(L/G) groups, so at most one slot per
     // (b, head) is untouched; the last slab's CTA writes it.
     const int nranks = rank == ULP_ALL_RANKS ? world_size : 1;
-    if (a.nq > 65535 || (long long)nranks * B > 65535)
-        return fail(ULP_EINVAL, "pack: grid too large (slots %d, ranks x batch %lld)", a.nq,
+    const int nslab = slots(L, kSlab);
+    if (nslab > 65535 || (long long)nranks * B > 65535)
+        return fail(ULP_EINVAL, "pack: grid too large (slabs %d, ranks x batch %lld)", nslab,
                     (long long)nranks * B);
-    const dim3 grid((unsigned)H, (unsigned)a.nq, (unsigned)(nranks * B));
+    const dim3 grid((unsigned)H, (unsigned)nslab, (unsigned)(nranks * B));
     const cudaStream_t st = (cudaStream_t)stream;
     const bool pdl = pdl_enabled(enable_pdl);
     a.early = enable_pdl == 2;
-    if (D == 128) {
-        if (dtype == ULP_BF16) launch_kernel(pack_kernel<128, ULP_BF16>, grid, dim3(kPackThreads), st, pdl, a);
-        else launch_kernel(pack_kernel<128, ULP_FP16>, grid, dim3(kPackThreads), st, pdl, a);
-    } else {
-        if (dtype == ULP_BF16) launch_kernel(pack_kernel<64, ULP_BF16>, grid, dim3(kPackThreads), st, pdl, a);
-        else launch_kernel(pack_kernel<64, ULP_FP16>, grid, dim3(kPackThreads), st, pdl, a);
-    }
+#define ULP_PACK_LAUNCH(GQ_)                                                                         \
+    do {                                                                                             \
+        if (D == 128) {                                                                              \
+            if (dtype == ULP_BF16) launch_kernel(pack_kernel<128, ULP_BF16, GQ_>, grid, dim3(kPackThreads), st, pdl, a); \
+            else launch_kernel(pack_kernel<128, ULP_FP16, GQ_>, grid, dim3(kPackThreads), st, pdl, a);                   \
+        } else {                                                                                     \
+            if (dtype == ULP_BF16) launch_kernel(pack_kernel<64, ULP_BF16, GQ_>, grid, dim3(kPackThreads), st, pdl, a);  \
+            else launch_kernel(pack_kernel<64, ULP_FP16, GQ_>, grid, dim3(kPackThreads), st, pdl, a);                    \
+        }                                                                                            \
+    } while (0)
+    if (q_group == 128) ULP_PACK_LAUNCH(128);
+    else ULP_PACK_LAUNCH(64);
+#undef ULP_PACK_LAUNCH
     return check_launch("pack");
 }

@@ -25,6 +25,7 @@ struct UnpackArgs {
     float *qs, *ks;
     ChunkLayout lay;
     int B, L, h, P, S, Spad, wq, wk, nq, nk, nd;
+    int gq;                    // Q group rows, 64 or 128
     int TT, CC;                // V tiles: t-tiles of 128 rows, 64-byte column blocks
     long long nVtiles, nVblk;  // V warp tiles, V blocks
     long long pieces, nCblk;   // copy pieces per span, copy blocks
@@ -140,9 +141,9 @@ __global__ void __launch_bounds__(kUnpackThreads) unpack_kernel(UnpackArgs a)
     int g = (int)(rem % (a.wq + a.wk));
     const uint8_t *rp = a.recv + (size_t)p * a.P * cbytes;
     if (g < a.wq) {
-        const int s = (g * kGQ) / a.L;
+        const int s = (g * a.gq) / a.L;
         const float *src = reinterpret_cast<const float *>(rp + (size_t)s * cbytes + a.lay.qs);
-        a.qs[((size_t)p * a.B * a.h + bj) * a.wq + g] = src[(size_t)bj * a.nq + (g - first_group(s, a.L, kGQ))];
+        a.qs[((size_t)p * a.B * a.h + bj) * a.wq + g] = src[(size_t)bj * a.nq + (g - first_group(s, a.L, a.gq))];
     } else {
         g -= a.wq;
         const int s = (g * kGK) / a.L;
@@ -156,11 +157,12 @@ __global__ void __launch_bounds__(kUnpackThreads) unpack_kernel(UnpackArgs a)
 using namespace ulp;
 
 extern "C" int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int D, int world_size,
-                                   int aligned, int scale_sequence, int8_t *q8, int8_t *k8,
-                                   uint8_t *v8, float *q_scale, float *k_scale, int num_dests,
-                                   int enable_pdl, ulp_stream_t stream)
+                                   int aligned, int scale_sequence, int q_group, int8_t *q8,
+                                   int8_t *k8, uint8_t *v8, float *q_scale, float *k_scale,
+                                   int num_dests, int enable_pdl, ulp_stream_t stream)
 {
     if (int s = check_world(world_size)) return s;
+    if (int s = check_q_group(q_group, "unpack")) return s;
     if (B < 1 || L < 1 || h < 1) return fail(ULP_EINVAL, "unpack: B, L, h must be positive (%d, %d, %d)", B, L, h);
     if (D != 64 && D != 128) return fail(ULP_EINVAL, "unpack: head_dim must be 64 or 128 (got %d)", D);
     if (num_dests < 1) return fail(ULP_EINVAL, "unpack: num_dests must be >= 1 (got %d)", num_dests);
@@ -178,12 +180,13 @@ extern "C" int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int
 
     UnpackArgs a{};
     a.recv = recv; a.q8 = q8; a.k8 = k8; a.v8 = v8; a.qs = q_scale; a.ks = k_scale;
-    a.lay = chunk_layout(B, L, h, D);
+    a.lay = chunk_layout(B, L, h, D, q_group);
+    a.gq = q_group;
     a.B = B; a.L = L; a.h = h; a.P = world_size; a.S = S; a.Spad = (S + 63) / 64 * 64;
     const int n = scale_sequence < 0 ? S : scale_sequence;
-    a.wq = (n + kGQ - 1) / kGQ;
+    a.wq = (n + q_group - 1) / q_group;
     a.wk = (n + kGK - 1) / kGK;
-    a.nq = slots(L, kGQ);
+    a.nq = slots(L, q_group);
     a.nk = slots(L, kGK);
     a.nd = num_dests;
     a.TT = (a.Spad + 127) / 128;

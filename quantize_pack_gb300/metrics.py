@@ -24,17 +24,19 @@ def _a16(x: int) -> int:
 
 def chunk_bytes(wl: Workload) -> int:
     n = wl.B * wl.L * wl.h * wl.D
-    return 3 * _a16(n) + _a16(4 * wl.B * wl.h * _slots(wl.L, 128)) + _a16(4 * wl.B * wl.h * _slots(wl.L, 64))
+    return (3 * _a16(n) + _a16(4 * wl.B * wl.h * _slots(wl.L, wl.q_group))
+            + _a16(4 * wl.B * wl.h * _slots(wl.L, 64)))
 
 
 def scale_section_bytes(wl: Workload) -> int:
     """Scale bytes of all P*P chunks."""
-    return wl.P * wl.P * 4 * wl.B * wl.h * (_slots(wl.L, 128) + _slots(wl.L, 64))
+    return wl.P * wl.P * 4 * wl.B * wl.h * (_slots(wl.L, wl.q_group) + _slots(wl.L, 64))
 
 
 def out_scale_bytes(wl: Workload) -> int:
     n = wl.S if wl.scale_sequence is None else wl.scale_sequence
-    return wl.P * 4 * wl.B * wl.h * ((n + 127) // 128 + (n + 63) // 64)
+    G = wl.q_group
+    return wl.P * 4 * wl.B * wl.h * ((n + G - 1) // G + (n + 63) // 64)
 
 
 def pack_bytes(wl: Workload) -> int:

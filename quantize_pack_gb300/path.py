@@ -25,7 +25,8 @@ from . import ulp
 class UlyssesLowpPath:
     def __init__(self, *, B: int, L: int, H: int, D: int, world_size: int, dtype: torch.dtype,
                  used_sequence: Optional[int] = None, scale_sequence: Optional[int] = None,
-                 aligned: Optional[bool] = None, fused: bool = True, fold_exchange: bool = True,
+                 aligned: Optional[bool] = None, q_group: int = ulp.GQ, fused: bool = True,
+                 fold_exchange: bool = True,
                  pdl: Optional[bool] = None, pdl_unpack: Optional[bool] = None, device="cuda"):
         P = world_size
         self.B, self.L, self.H, self.D, self.P = B, L, H, D, P
@@ -35,6 +36,7 @@ class UlyssesLowpPath:
         self.used_sequence = used_sequence
         self.scale_sequence = scale_sequence
         self.aligned = aligned
+        self.q_group = q_group
         self.fused = fused
         self.fold_exchange = fold_exchange
         # pdl: programmatic launch of pack, which follows derive (derive writes
@@ -44,7 +46,7 @@ class UlyssesLowpPath:
         self.pdl_pack = 2 if pdl is None or pdl else 0
         self.pdl = bool(pdl_unpack)
         self.device = torch.device(device)
-        self.chunk_bytes = ulp.chunk_bytes(B, L, self.h, D)
+        self.chunk_bytes = ulp.chunk_bytes(B, L, self.h, D, q_group)
         f32 = dict(dtype=torch.float32, device=self.device)
         self.k_amax = torch.empty((P, B, H, ulp.slots(L, ulp.GK)), **f32)
         self.minmax = torch.empty((P, B, H, 2, 2, D), **f32)
@@ -52,7 +54,8 @@ class UlyssesLowpPath:
         u8 = dict(dtype=torch.uint8, device=self.device)
         self.recv = torch.empty((P, P, self.chunk_bytes), **u8)
         self.send = None if fold_exchange else torch.empty((P, P, self.chunk_bytes), **u8)
-        self.out = ulp.unpack_outputs(B, L, self.h, D, P, scale_sequence, self.device, num_dests=P)
+        self.out = ulp.unpack_outputs(B, L, self.h, D, P, scale_sequence, self.device, num_dests=P,
+                                      q_group=q_group)
 
     @property
     def launches_per_step(self) -> int:
@@ -74,19 +77,19 @@ class UlyssesLowpPath:
             ulp.k_grouped_amax(k, k_mean, rank=None, world_size=P,
                                used_sequence=self.used_sequence, out=self.k_amax)
         ulp.boundary_minmax(k, q, rank=None, world_size=P, used_sequence=self.used_sequence,
-                            out=(self.minmax, self.q_partial))
+                            q_group=self.q_group, out=(self.minmax, self.q_partial))
         ulp.derive_k_boundary_amax(self.k_amax, self.minmax, k_mean, rank=None, local_sequence=L,
                                    world_size=P)
         if on_pack is not None:
             on_pack[0]()
         if self.fold_exchange:
             ulp.pack(q, k, v, k_mean, self.k_amax, self.q_partial, v_scale, rank=None,
-                     world_size=P, used_sequence=self.used_sequence, fused=self.fused,
-                     send=self.recv, send_layout=ulp.SEND_DEST_MAJOR, enable_pdl=self.pdl_pack)
+                     world_size=P, used_sequence=self.used_sequence, q_group=self.q_group,
+                     fused=self.fused, send=self.recv, send_layout=ulp.SEND_DEST_MAJOR, enable_pdl=self.pdl_pack)
         else:
             ulp.pack(q, k, v, k_mean, self.k_amax, self.q_partial, v_scale, rank=None,
-                     world_size=P, used_sequence=self.used_sequence, fused=self.fused,
-                     send=self.send, send_layout=ulp.SEND_SOURCE_MAJOR, enable_pdl=self.pdl_pack)
+                     world_size=P, used_sequence=self.used_sequence, q_group=self.q_group,
+                     fused=self.fused, send=self.send, send_layout=ulp.SEND_SOURCE_MAJOR, enable_pdl=self.pdl_pack)
         if on_pack is not None:
             on_pack[1]()
         if not self.fold_exchange:
@@ -94,7 +97,7 @@ class UlyssesLowpPath:
         return ulp.unpack_for_sage(self.recv, batch_size=self.B, local_sequence=L,
                                    local_heads=self.h, head_dim=self.D, world_size=P,
                                    aligned=self.aligned, scale_sequence=self.scale_sequence,
-                                   out=self.out, enable_pdl=self.pdl)
+                                   q_group=self.q_group, out=self.out, enable_pdl=self.pdl)
 
     def capture(self, q, k, v, k_mean, v_scale):
         """Record one step on these input tensors as a CUDA graph; replay it

@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libulp.so")
 ULP_BF16, ULP_FP16 = 0, 1
 ULP_ALL_RANKS = -1
 SEND_SOURCE_MAJOR, SEND_DEST_MAJOR = 0, 1
-GK, GQ = 64, 128
+GK, GQ = 64, 128   # K group rows; default Q group rows (q_group=64 selects the other width)
 
 _STATUS = {-1: "EINVAL", -2: "EDTYPE", -3: "EALIGN", -4: "ECUDA"}
 
@@ -54,20 +54,20 @@ def lib() -> ctypes.CDLL:
         L.ulp_last_error.restype = ctypes.c_char_p
         L.ulp_last_error.argtypes = []
         L.ulp_slots.argtypes = [_I, _I]
-        L.ulp_scale_widths.argtypes = [_I, ctypes.POINTER(_I), ctypes.POINTER(_I)]
-        L.ulp_chunk_bytes.argtypes = [_I, _I, _I, _I, ctypes.POINTER(_SZ)]
-        L.ulp_chunk_offsets.argtypes = [_I, _I, _I, _I, ctypes.POINTER(_SZ)]
+        L.ulp_scale_widths.argtypes = [_I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]
+        L.ulp_chunk_bytes.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]
+        L.ulp_chunk_offsets.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]
         L.ulp_k_mean_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]
         L.ulp_k_mean_global.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _P]
         L.ulp_k_mean_global_noalloc.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P]
         L.ulp_k_grouped_amax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P]
-        L.ulp_boundary_minmax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]
+        L.ulp_boundary_minmax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]
         L.ulp_derive_k_boundary_amax.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]
-        L.ulp_pack.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P,
-                               _I, _I, _P]
+        L.ulp_pack.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                               _P, _I, _I, _P]
         L.ulp_alltoall_emulate.argtypes = [_P, _P, _I, _SZ, _P]
-        L.ulp_unpack_for_sage.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I,
-                                          _I, _P]
+        L.ulp_unpack_for_sage.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
+                                          _I, _I, _P]
         for name in ("ulp_slots", "ulp_scale_widths", "ulp_chunk_bytes", "ulp_chunk_offsets",
                      "ulp_k_mean_workspace_bytes", "ulp_k_mean_global", "ulp_k_mean_global_noalloc",
                      "ulp_k_grouped_amax", "ulp_boundary_minmax", "ulp_derive_k_boundary_amax",
@@ -129,22 +129,22 @@ def slots(L: int, G: int) -> int:
     return _check(lib().ulp_slots(L, G))
 
 
-def scale_widths(n: int) -> Tuple[int, int]:
+def scale_widths(n: int, q_group: int = GQ) -> Tuple[int, int]:
     """(Q width, K width) of the consumer scale tensors for n rows."""
     q, k = _I(), _I()
-    _check(lib().ulp_scale_widths(n, ctypes.byref(q), ctypes.byref(k)))
+    _check(lib().ulp_scale_widths(n, q_group, ctypes.byref(q), ctypes.byref(k)))
     return q.value, k.value
 
 
-def chunk_bytes(B: int, L: int, h: int, D: int) -> int:
+def chunk_bytes(B: int, L: int, h: int, D: int, q_group: int = GQ) -> int:
     n = _SZ()
-    _check(lib().ulp_chunk_bytes(B, L, h, D, ctypes.byref(n)))
+    _check(lib().ulp_chunk_bytes(B, L, h, D, q_group, ctypes.byref(n)))
     return n.value
 
 
-def chunk_offsets(B: int, L: int, h: int, D: int) -> Tuple[int, ...]:
+def chunk_offsets(B: int, L: int, h: int, D: int, q_group: int = GQ) -> Tuple[int, ...]:
     arr = (_SZ * 5)()
-    _check(lib().ulp_chunk_offsets(B, L, h, D, arr))
+    _check(lib().ulp_chunk_offsets(B, L, h, D, q_group, arr))
     return tuple(int(x) for x in arr)
 
 
@@ -216,7 +216,7 @@ def k_grouped_amax(k: torch.Tensor, k_mean_global: torch.Tensor, *, rank: Option
 
 
 def boundary_minmax(k: torch.Tensor, q: torch.Tensor, *, rank: Optional[int], world_size: int,
-                    used_sequence: Optional[int] = None,
+                    used_sequence: Optional[int] = None, q_group: int = GQ,
                     out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
     """Raw-K boundary min/max [B, H, 2, 2, D] and Q boundary partial amax
     [B, H, 2] of a rank (stacked over ranks for rank=None: the gathered
@@ -229,7 +229,8 @@ def boundary_minmax(k: torch.Tensor, q: torch.Tensor, *, rank: Optional[int], wo
     else:
         mm, qp = out
     _check(lib().ulp_boundary_minmax(_ptr(k), _ptr(q), _dtype_code(k), B, L, H, D, rc, world_size,
-                                     _opt(used_sequence), _ptr(mm), _ptr(qp), _stream(k.device)))
+                                     _opt(used_sequence), q_group, _ptr(mm), _ptr(qp),
+                                     _stream(k.device)))
     return mm, qp
 
 
@@ -250,13 +251,13 @@ def derive_k_boundary_amax(grouped_amax: torch.Tensor, gathered_minmax: torch.Te
 def pack(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, k_mean_global: torch.Tensor,
          k_amax: torch.Tensor, gathered_q_partial: torch.Tensor, v_scale: torch.Tensor, *,
          rank: Optional[int], world_size: int, used_sequence: Optional[int] = None,
-         fused: bool = True, send: Optional[torch.Tensor] = None,
+         q_group: int = GQ, fused: bool = True, send: Optional[torch.Tensor] = None,
          send_layout: int = SEND_SOURCE_MAJOR,
          enable_pdl=None) -> torch.Tensor:
     """Quantise a rank's Q/K/V into its P chunks (INT8 Q/K, FP8 E4M3 V)."""
     rc, nr, B, L, H, D = _rank_dims(q, rank)
     h = H // world_size
-    cb = chunk_bytes(B, L, h, D)
+    cb = chunk_bytes(B, L, h, D, q_group)
     if send is None:
         if send_layout == SEND_DEST_MAJOR:
             shape = (world_size, world_size, cb)
@@ -265,7 +266,7 @@ def pack(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, k_mean_global: torch
         send = torch.empty(shape, dtype=torch.uint8, device=q.device)
     _check(lib().ulp_pack(_ptr(q), _ptr(k), _ptr(v), _ptr(k_mean_global), _dtype_code(q),
                           _ptr(k_amax), _ptr(gathered_q_partial), _ptr(v_scale), B, L, H, D, rc,
-                          world_size, _opt(used_sequence), int(bool(fused)), _ptr(send),
+                          world_size, _opt(used_sequence), q_group, int(bool(fused)), _ptr(send),
                           int(send_layout), _pdl(enable_pdl), _stream(q.device)))
     return send
 
@@ -281,11 +282,11 @@ def alltoall_emulate(send: torch.Tensor, recv: Optional[torch.Tensor] = None) ->
 
 def unpack_outputs(batch_size: int, local_sequence: int, local_heads: int, head_dim: int,
                    world_size: int, scale_sequence: Optional[int], device,
-                   num_dests: Optional[int] = None):
+                   num_dests: Optional[int] = None, q_group: int = GQ):
     B, L, h, D, P = batch_size, local_sequence, local_heads, head_dim, world_size
     S = P * L
     Spad = (S + 63) // 64 * 64
-    wq, wk = scale_widths(S if scale_sequence is None else scale_sequence)
+    wq, wk = scale_widths(S if scale_sequence is None else scale_sequence, q_group)
     lead = () if num_dests is None else (num_dests,)
     return (torch.empty(lead + (B, S, h, D), dtype=torch.int8, device=device),
             torch.empty(lead + (B, S, h, D), dtype=torch.int8, device=device),
@@ -297,7 +298,7 @@ def unpack_outputs(batch_size: int, local_sequence: int, local_heads: int, head_
 def unpack_for_sage(recv_u8: torch.Tensor, *, batch_size: int, local_sequence: int,
                     local_heads: int, head_dim: int, world_size: int,
                     aligned: Optional[bool] = None, scale_sequence: Optional[int] = None,
-                    out: Optional[Sequence[torch.Tensor]] = None,
+                    q_group: int = GQ, out: Optional[Sequence[torch.Tensor]] = None,
                     enable_pdl: Optional[bool] = None):
     """Unpack source chunks onto the global grid (page "unpack_for_sage").
 
@@ -309,12 +310,12 @@ def unpack_for_sage(recv_u8: torch.Tensor, *, batch_size: int, local_sequence: i
     nd = None if recv_u8.dim() == 2 else recv_u8.shape[0]
     if out is None:
         out = unpack_outputs(batch_size, local_sequence, local_heads, head_dim, world_size,
-                             scale_sequence, recv_u8.device, nd)
+                             scale_sequence, recv_u8.device, nd, q_group)
     q8, k8, v8, qs, ks = out
     v8b = v8.view(torch.uint8) if v8.dtype != torch.uint8 else v8
     _check(lib().ulp_unpack_for_sage(_ptr(recv_u8), batch_size, local_sequence, local_heads,
                                      head_dim, world_size, _tri(aligned), _opt(scale_sequence),
-                                     _ptr(q8), _ptr(k8), _ptr(v8b), _ptr(qs), _ptr(ks),
+                                     q_group, _ptr(q8), _ptr(k8), _ptr(v8b), _ptr(qs), _ptr(ks),
                                      1 if nd is None else nd, _pdl(enable_pdl),
                                      _stream(recv_u8.device)))
     return tuple(out)

@@ -47,8 +47,14 @@ USED1 = configs.Workload("used1_P4_L50", B=1, H=8, D=64, P=4, L=50, dtype=config
 B3 = configs.Workload("b3_P2_L300_D64_fp16", B=3, H=6, D=64, P=2, L=300, dtype=configs.FP16,
                       seed=17, pad_rows=45, k_mean_std=3.0, k_noise_std=0.1, qv_dist="t3")
 
+# the q_group = 64 variant (Q groups are the K groups) on the geometries with
+# the most boundary cases: groups over 4 and 8 ranks, one-row shards, the
+# partial live group across ranks, world_size 6, a ragged non-aligned shard
+G64 = [w.replace(q_group=64, name=w.name + "_gq64") for w in (TINY, LONG_R, SPAN4_PAD, L1,
+                                                              CROSS_PAD, SIX, B3)]
+
 CPU_WORKLOADS = [TINY, PADDING_R, VIDEO_R, LONG_R, HEAVY_R, SPAN4, SPAN4_PAD, L1, CROSS_PAD, SIX,
-                 USED64, USED1, B3]
+                 USED64, USED1, B3] + G64
 
 
 def f32(bits: np.ndarray, dtype: int) -> np.ndarray:
@@ -83,13 +89,15 @@ def global_k_amax(inp: synth.Inputs) -> np.ndarray:
 
 
 def global_q_amax(inp: synth.Inputs) -> np.ndarray:
-    """max(1e-7, max |Q|) over each global 128-row group.  [B, H, ceil(S/128)]."""
+    """max(1e-7, max |Q|) over each global G-row group, G = the workload's
+    q_group.  [B, H, ceil(S/G)]."""
     wl = inp.wl
+    G = wl.q_group
     qa = np.abs(f32(inp.q, wl.dtype))
-    ng = (wl.S + 127) // 128
+    ng = (wl.S + G - 1) // G
     out = np.empty((wl.B, wl.H, ng), np.float32)
     for g in range(ng):
-        out[:, :, g] = np.maximum(qa[:, g * 128:g * 128 + 128].max(axis=(1, 3)), EPS)
+        out[:, :, g] = np.maximum(qa[:, g * G:g * G + G].max(axis=(1, 3)), EPS)
     return out
 
 
@@ -111,7 +119,7 @@ def run_oracle(inp: synth.Inputs, dests=None):
     wl = inp.wl
     return O.forward(inp.shards("q"), inp.shards("k"), inp.shards("v"), inp.k_mean, inp.v_scale,
                      wl.dtype, used_sequence=wl.used_sequence, scale_sequence=wl.scale_sequence,
-                     dests=dests)
+                     dests=dests, q_group=wl.q_group)
 
 
 _cache = {}

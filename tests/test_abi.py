@@ -37,14 +37,20 @@ def test_geometry_agrees_with_oracle(lib):
     for L in list(range(1, 400)) + [1000, 4096, 9360, 16384]:
         for G in (64, 128):
             assert ulp.slots(L, G) == O.slots(L, G)
-    for n in range(1, 1200):
-        assert ulp.scale_widths(n) == O.scale_widths(n)
-    for Bb, L, h, D in [(1, 96, 4, 64), (1, 1000, 4, 128), (2, 4096, 3, 128), (1, 9360, 5, 128),
-                        (4, 16384, 16, 64), (3, 17, 3, 64), (2, 1, 1, 128)]:
-        lay = O.chunk_layout(Bb, L, h, D)
-        assert ulp.chunk_bytes(Bb, L, h, D) == lay["chunk_bytes"]
-        assert ulp.chunk_offsets(Bb, L, h, D) == (lay["q"], lay["k"], lay["v"], lay["q_scale"],
-                                                 lay["k_scale"])
+    for G_Q in (64, 128):
+        for n in range(1, 1200):
+            assert ulp.scale_widths(n, G_Q) == O.scale_widths(n, G_Q)
+        for Bb, L, h, D in [(1, 96, 4, 64), (1, 1000, 4, 128), (2, 4096, 3, 128), (1, 9360, 5, 128),
+                            (4, 16384, 16, 64), (3, 17, 3, 64), (2, 1, 1, 128)]:
+            lay = O.chunk_layout(Bb, L, h, D, G_Q)
+            assert ulp.chunk_bytes(Bb, L, h, D, G_Q) == lay["chunk_bytes"]
+            assert ulp.chunk_offsets(Bb, L, h, D, G_Q) == (lay["q"], lay["k"], lay["v"],
+                                                          lay["q_scale"], lay["k_scale"])
+    for bad in (0, 32, 96, 256):
+        with pytest.raises(ulp.UlpError):
+            ulp.scale_widths(100, bad)
+        with pytest.raises(ulp.UlpError):
+            ulp.chunk_bytes(1, 96, 4, 64, bad)
 
 
 FAKE = 1 << 20   # an aligned, never-dereferenced address: every call below fails validation
@@ -72,27 +78,30 @@ def test_k_grouped_amax_rejects(lib, args, status):
 
 
 def test_unpack_rejects(lib):
-    ok = dict(recv=FAKE, B=1, L=96, h=4, D=64, P=2, aligned=-1, sseq=-1, q8=FAKE, k8=FAKE,
-              v8=FAKE, qs=FAKE, ks=FAKE, nd=1, pdl=-1)
+    ok = dict(recv=FAKE, B=1, L=96, h=4, D=64, P=2, aligned=-1, sseq=-1, gq=128, q8=FAKE,
+              k8=FAKE, v8=FAKE, qs=FAKE, ks=FAKE, nd=1, pdl=-1)
 
     def call(**kw):
         a = dict(ok, **kw)
         return lib.ulp_unpack_for_sage(a["recv"], a["B"], a["L"], a["h"], a["D"], a["P"],
-                                       a["aligned"], a["sseq"], a["q8"], a["k8"], a["v8"],
+                                       a["aligned"], a["sseq"], a["gq"], a["q8"], a["k8"], a["v8"],
                                        a["qs"], a["ks"], a["nd"], a["pdl"], None)
     assert call(aligned=1) == -1                       # L % 128 != 0
     assert b"aligned" in lib.ulp_last_error()
     assert call(sseq=0) == -1 and call(sseq=193) == -1
     assert call(P=5) == -1 and call(D=32) == -1 and call(nd=0) == -1
     assert call(v8=FAKE + 1) == -3
+    assert call(gq=96) == -1 and b"q_group" in lib.ulp_last_error()
 
 
 def test_pack_and_derive_reject(lib):
     base = [FAKE] * 8
-    # fused must be 0/1, send_layout 0/1
-    assert lib.ulp_pack(*base[:4], 0, *base[4:7], 1, 96, 8, 64, 0, 2, -1, 2, FAKE, 0, -1, None) == -1
-    assert lib.ulp_pack(*base[:4], 0, *base[4:7], 1, 96, 8, 64, 0, 2, -1, 1, FAKE, 3, -1, None) == -1
-    assert lib.ulp_pack(*base[:4], 0, *base[4:7], 1, 96, 8, 64, 0, 2, -1, 1, FAKE + 2, 0, -1, None) == -3
+    # fused must be 0/1, send_layout 0/1, q_group 64/128
+    assert lib.ulp_pack(*base[:4], 0, *base[4:7], 1, 96, 8, 64, 0, 2, -1, 128, 2, FAKE, 0, -1, None) == -1
+    assert lib.ulp_pack(*base[:4], 0, *base[4:7], 1, 96, 8, 64, 0, 2, -1, 128, 1, FAKE, 3, -1, None) == -1
+    assert lib.ulp_pack(*base[:4], 0, *base[4:7], 1, 96, 8, 64, 0, 2, -1, 128, 1, FAKE + 2, 0, -1, None) == -3
+    assert lib.ulp_pack(*base[:4], 0, *base[4:7], 1, 96, 8, 64, 0, 2, -1, 32, 1, FAKE, 0, -1, None) == -1
     assert lib.ulp_derive_k_boundary_amax(FAKE, FAKE, FAKE, 1, 1, 8, 64, 2, 96, 2, None) == -1
-    assert lib.ulp_boundary_minmax(FAKE, FAKE, 0, 1, 96, 8, 64, 0, 2, 500, FAKE, FAKE, None) == -1
+    assert lib.ulp_boundary_minmax(FAKE, FAKE, 0, 1, 96, 8, 64, 0, 2, 500, 128, FAKE, FAKE, None) == -1
+    assert lib.ulp_boundary_minmax(FAKE, FAKE, 0, 1, 96, 8, 64, 0, 2, -1, 0, FAKE, FAKE, None) == -1
     assert lib.ulp_alltoall_emulate(FAKE, FAKE, 2, 24, None) == -1

@@ -30,7 +30,8 @@ def guards_intact(buf):
     return bool(np.all(b[:GUARD] == PATTERN) and np.all(b[-GUARD:] == PATTERN))
 
 
-@pytest.mark.parametrize("wl", [hp.TINY, hp.SPAN4_PAD, hp.SIX, hp.LONG_R, hp.B3], ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", [hp.TINY, hp.SPAN4_PAD, hp.SIX, hp.LONG_R, hp.B3, hp.G64[2], hp.G64[5]],
+                         ids=lambda w: w.name)
 def test_outputs_have_untouched_guards(wl):
     inp, res, (q, k, v, km, vs) = _setup(wl)
     P, B, L, H, D = wl.P, wl.B, wl.L, wl.H, wl.D
@@ -39,19 +40,23 @@ def test_outputs_have_untouched_guards(wl):
     ulp.k_grouped_amax(k, km, rank=None, world_size=P, used_sequence=wl.used_sequence, out=ga)
     mm_buf, mm = guarded((P, B, H, 2, 2, D), torch.float32)
     qp_buf, qp = guarded((P, B, H, 2), torch.float32)
-    ulp.boundary_minmax(k, q, rank=None, world_size=P, used_sequence=wl.used_sequence, out=(mm, qp))
+    G_Q = wl.q_group
+    ulp.boundary_minmax(k, q, rank=None, world_size=P, used_sequence=wl.used_sequence, q_group=G_Q,
+                        out=(mm, qp))
     ulp.derive_k_boundary_amax(ga, mm, km, rank=None, local_sequence=L, world_size=P)
-    cb = ulp.chunk_bytes(B, L, wl.h, D)
+    cb = ulp.chunk_bytes(B, L, wl.h, D, G_Q)
     send_buf, send = guarded((P, P, cb), torch.uint8)
     ulp.pack(q, k, v, km, ga, qp, vs, rank=None, world_size=P, used_sequence=wl.used_sequence,
-             fused=False, send=send)
+             q_group=G_Q, fused=False, send=send)
     recv_buf, recv = guarded((P, P, cb), torch.uint8)
     ulp.alltoall_emulate(send, recv)
-    shapes = [o.shape for o in ulp.unpack_outputs(B, L, wl.h, D, P, wl.scale_sequence, "cuda", P)]
+    shapes = [o.shape for o in ulp.unpack_outputs(B, L, wl.h, D, P, wl.scale_sequence, "cuda", P,
+                                                  q_group=G_Q)]
     dts = [torch.int8, torch.int8, torch.uint8, torch.float32, torch.float32]
     outs = [guarded(s, d) for s, d in zip(shapes, dts)]
     ulp.unpack_for_sage(recv, batch_size=B, local_sequence=L, local_heads=wl.h, head_dim=D,
-                        world_size=P, scale_sequence=wl.scale_sequence, out=[o[1] for o in outs])
+                        world_size=P, scale_sequence=wl.scale_sequence, q_group=G_Q,
+                        out=[o[1] for o in outs])
     torch.cuda.synchronize()
     for name, buf in [("amax", ga_buf), ("minmax", mm_buf), ("q partial", qp_buf), ("send", send_buf),
                       ("recv", recv_buf)] + [(f"out{i}", o[0]) for i, o in enumerate(outs)]:

@@ -34,12 +34,13 @@ def test_k_grouped_amax(wl):
 @pytest.mark.parametrize("wl", GPU_WORKLOADS, ids=lambda w: w.name)
 def test_boundary_minmax(wl):
     inp, res, (q, k, v, km, vs) = _setup(wl)
-    mm, qp = ulp.boundary_minmax(k, q, rank=None, world_size=wl.P, used_sequence=wl.used_sequence)
+    mm, qp = ulp.boundary_minmax(k, q, rank=None, world_size=wl.P, used_sequence=wl.used_sequence,
+                                 q_group=wl.q_group)
     gh.assert_bits_equal(mm, res["minmax"], "minmax")
     gh.assert_bits_equal(qp, res["qb"], "q partial")
     r = wl.P - 1
     mm1, qp1 = ulp.boundary_minmax(k[r].contiguous(), q[r].contiguous(), rank=r, world_size=wl.P,
-                                   used_sequence=wl.used_sequence)
+                                   used_sequence=wl.used_sequence, q_group=wl.q_group)
     gh.assert_bits_equal(mm1, res["minmax"][r], "minmax one rank")
     gh.assert_bits_equal(qp1, res["qb"][r], "q partial one rank")
 
@@ -48,7 +49,8 @@ def test_boundary_minmax(wl):
 def test_derive(wl):
     inp, res, (q, k, v, km, vs) = _setup(wl)
     ga = ulp.k_grouped_amax(k, km, rank=None, world_size=wl.P, used_sequence=wl.used_sequence)
-    mm, _ = ulp.boundary_minmax(k, q, rank=None, world_size=wl.P, used_sequence=wl.used_sequence)
+    mm, _ = ulp.boundary_minmax(k, q, rank=None, world_size=wl.P, used_sequence=wl.used_sequence,
+                                 q_group=wl.q_group)
     ulp.derive_k_boundary_amax(ga, mm, km, rank=None, local_sequence=wl.L, world_size=wl.P)
     gh.assert_bits_equal(ga, res["amax"], "derived amax (all ranks)")
     # one rank at a time, from the oracle's own kernel output and gather
@@ -69,21 +71,22 @@ def test_pack(wl, fused):
         ga = torch.full((P, wl.B, wl.H, ulp.slots(wl.L, 64)), float("nan"), device="cuda")
     else:
         ga = ulp.k_grouped_amax(k, km, rank=None, world_size=P, used_sequence=wl.used_sequence)
-    mm, qp = ulp.boundary_minmax(k, q, rank=None, world_size=P, used_sequence=wl.used_sequence)
+    mm, qp = ulp.boundary_minmax(k, q, rank=None, world_size=P, used_sequence=wl.used_sequence,
+                                 q_group=wl.q_group)
     ulp.derive_k_boundary_amax(ga, mm, km, rank=None, local_sequence=wl.L, world_size=P)
     send = ulp.pack(q, k, v, km, ga, qp, vs, rank=None, world_size=P,
-                    used_sequence=wl.used_sequence, fused=fused)
+                    used_sequence=wl.used_sequence, q_group=wl.q_group, fused=fused)
     gh.assert_bits_equal(send, res["send"], "send (source-major)")
     gh.assert_bits_equal(ga, res["amax"], "k_amax after pack")
     recv = ulp.pack(q, k, v, km, ga, qp, vs, rank=None, world_size=P,
-                    used_sequence=wl.used_sequence, fused=fused,
+                    used_sequence=wl.used_sequence, q_group=wl.q_group, fused=fused,
                     send_layout=ulp.SEND_DEST_MAJOR)
     gh.assert_bits_equal(recv, res["recv"], "send (dest-major) = recv")
     # single-rank calls write the same chunks
     r = P - 1
     one = ulp.pack(q[r].contiguous(), k[r].contiguous(), v[r].contiguous(), km,
                    ga[r].contiguous(), qp, vs, rank=r, world_size=P,
-                   used_sequence=wl.used_sequence, fused=fused)
+                   used_sequence=wl.used_sequence, q_group=wl.q_group, fused=fused)
     gh.assert_bits_equal(one, res["send"][r], f"send rank {r}")
 
 
@@ -96,7 +99,7 @@ def test_alltoall_and_unpack(wl):
     gh.assert_bits_equal(recv, res["recv"], "recv")
     outs = ulp.unpack_for_sage(recv, batch_size=wl.B, local_sequence=wl.L, local_heads=wl.h,
                                head_dim=wl.D, world_size=P, aligned=wl.aligned,
-                               scale_sequence=wl.scale_sequence)
+                               scale_sequence=wl.scale_sequence, q_group=wl.q_group)
     names = ["q8", "k8", "v8", "q_scale", "k_scale"]
     for i, name in enumerate(names):
         want = np.stack([res["out"][p][i] for p in range(P)])
@@ -105,7 +108,7 @@ def test_alltoall_and_unpack(wl):
     for p in sorted({0, P - 1}):
         one = ulp.unpack_for_sage(recv[p].contiguous(), batch_size=wl.B, local_sequence=wl.L,
                                   local_heads=wl.h, head_dim=wl.D, world_size=P,
-                                  scale_sequence=wl.scale_sequence)
+                                  scale_sequence=wl.scale_sequence, q_group=wl.q_group)
         for i, name in enumerate(names):
             gh.assert_bits_equal(one[i], res["out"][p][i], f"{name} dest {p}")
 
@@ -117,7 +120,8 @@ def test_whole_path(wl, mode):
     path = UlyssesLowpPath(B=wl.B, L=wl.L, H=wl.H, D=wl.D, world_size=wl.P,
                            dtype=gh.torch_dtype(wl.dtype), used_sequence=wl.used_sequence,
                            scale_sequence=wl.scale_sequence, aligned=wl.aligned,
-                           fused=(mode == "fused_folded"), fold_exchange=(mode == "fused_folded"))
+                           q_group=wl.q_group, fused=(mode == "fused_folded"),
+                           fold_exchange=(mode == "fused_folded"))
     for _ in range(2):                      # a second step on the same buffers
         outs = path.run(q, k, v, km, vs)
         torch.cuda.synchronize()

@@ -80,9 +80,10 @@ def test_minmax_and_q_partials(wl):
                 rows = kf[:, lo:hi] + np.float32(0)          # -0 -> +0
                 assert np.array_equal(mn, rows.min(axis=1))
                 assert np.array_equal(mx, rows.max(axis=1))
-            qg = hp.touched_groups(r, wl.L, 128)
+            G_Q = wl.q_group
+            qg = hp.touched_groups(r, wl.L, G_Q)
             gq = qg[0] if e == 0 else qg[-1]
-            lo, hi = max(gq * 128, r * wl.L), min(gq * 128 + 128, (r + 1) * wl.L)
+            lo, hi = max(gq * G_Q, r * wl.L), min(gq * G_Q + G_Q, (r + 1) * wl.L)
             want = np.maximum(qa[:, lo:hi].max(axis=(1, 3)), hp.EPS)
             assert np.array_equal(res["qb"][r][:, :, e], want)
 

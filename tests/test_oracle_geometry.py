@@ -51,22 +51,24 @@ def test_slots_bound_every_rank(G):
                 assert max(touched) == n
 
 
-def test_chunk_sections_aligned_and_disjoint():
+@pytest.mark.parametrize("G_Q", [64, 128])
+def test_chunk_sections_aligned_and_disjoint(G_Q):
     for B, L, h, D in [(1, 96, 4, 64), (1, 1000, 4, 128), (3, 17, 3, 64), (2, 1, 1, 128)]:
-        lay = O.chunk_layout(B, L, h, D)
+        lay = O.chunk_layout(B, L, h, D, G_Q)
         n = B * L * h * D
         assert lay["q"] == 0 and lay["k"] >= n and lay["v"] >= lay["k"] + n
         assert lay["q_scale"] >= lay["v"] + n
-        assert lay["k_scale"] >= lay["q_scale"] + 4 * B * h * O.slots(L, 128)
+        assert lay["k_scale"] >= lay["q_scale"] + 4 * B * h * O.slots(L, G_Q)
         assert lay["chunk_bytes"] >= lay["k_scale"] + 4 * B * h * O.slots(L, 64)
         for key in ("k", "v", "q_scale", "k_scale", "chunk_bytes"):
             assert lay[key] % 16 == 0
 
 
-def test_scale_widths_cover_prefix():
+@pytest.mark.parametrize("G_Q", [64, 128])
+def test_scale_widths_cover_prefix(G_Q):
     for n in range(1, 2000):
-        wq, wk = O.scale_widths(n)
-        assert (wq - 1) * 128 < n <= wq * 128
+        wq, wk = O.scale_widths(n, G_Q)
+        assert (wq - 1) * G_Q < n <= wq * G_Q
         assert (wk - 1) * 64 < n <= wk * 64
 
 

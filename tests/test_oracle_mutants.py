@@ -41,8 +41,12 @@ MUTANTS = {
                                       "                    float xk = in_f32(k_mean, ((size_t)b * H + hh) * D + d, dtype) - in_f32(k, src, dtype);"),
     "v not transposed": ("                    v8[vdst] = chunk[ov + src];",
                          "                    v8[(((size_t)b * Spad + t) * h + j) * D + d < (size_t)B * D * h * Spad ? (((size_t)b * Spad + t) * h + j) * D + d : vdst] = chunk[ov + src];"),
-    "q scale from the next slot": ("                q_scale[((size_t)b * h + j) * wq + g] = src[((size_t)b * h + j) * nq + (g - first_group(s, L, GQ))];",
-                                   "                q_scale[((size_t)b * h + j) * wq + g] = src[((size_t)b * h + j) * nq + (g - first_group(s, L, GQ)) + (g + 1 < wq)];"),
+    "q scale from the next slot": ("                q_scale[((size_t)b * h + j) * wq + g] = src[((size_t)b * h + j) * nq + (g - first_group(s, L, gq))];",
+                                   "                q_scale[((size_t)b * h + j) * wq + g] = src[((size_t)b * h + j) * nq + (g - first_group(s, L, gq)) + (g + 1 < wq)];"),
+    "64-row Q groups coded with the 128-row slot": ("                float sq = qs[t / gq - fq], sk = ks[t / GK - fk];",
+                                                    "                float sq = qs[t / gq - fq - (gq == 64 && (t / 64) % 2 == 1 && t / 64 > fq)], sk = ks[t / GK - fk];"),
+    "Q partial over 128 rows in the 64-row variant": ("                int qhi = g_q * gq + gq < row0 + L ? g_q * gq + gq : row0 + L;",
+                                                      "                int qhi = g_q * gq + 128 < row0 + L ? g_q * gq + 128 : row0 + L;"),
     "-0 kept in min/max": ("                        if (x == 0.0f) x = 0.0f;   /* -0 -> +0 */", ""),
 }
 
@@ -107,7 +111,7 @@ def pins_pass(wl, negzero=False) -> bool:
         qs = (hp.global_q_amax(inp) / np.float32(127)).astype(np.float32)
         if qsc.tobytes() != np.ascontiguousarray(qs[:, :, :qsc.shape[2]]).tobytes():
             return False
-        row_qs = np.repeat(qs, 128, axis=2)[:, :, :S].transpose(0, 2, 1)[..., None]
+        row_qs = np.repeat(qs, wl.q_group, axis=2)[:, :, :S].transpose(0, 2, 1)[..., None]
         if not np.array_equal(q8, hp.int8_codes(hp.f32(inp.q, wl.dtype), row_qs)):
             return False
         ksc = (direct / np.float32(127)).astype(np.float32)
@@ -143,7 +147,8 @@ INNER_PAD = hp.configs.Workload("inner_pad_P2_L300_used500", B=1, H=4, D=64, P=2
                                 dtype=hp.configs.BF16, seed=18, pad_rows=100, scale_to_used=True,
                                 k_mean_std=4.0, k_noise_std=0.05)
 WORKLOADS = [hp.CROSS_PAD, hp.SPAN4_PAD, hp.USED64.replace(H=8, name="used64_h2"),
-             hp.TINY, INNER_PAD]
+             hp.TINY, INNER_PAD, hp.SPAN4_PAD.replace(q_group=64, name="span4_pad_gq64"),
+             INNER_PAD.replace(q_group=64, name="inner_pad_gq64")]
 
 
 def _all_pass():

@@ -32,12 +32,12 @@ def test_p_invariance_against_global_quantisation(wl):
     qf, kf, vf = (hp.f32(getattr(inp, n), wl.dtype) for n in "qkv")
     m = hp.f32(inp.k_mean, wl.dtype)
 
-    # Q: scales and codes from the global 128-row group amax
+    # Q: scales and codes from the global q_group-row group amax
     qa = hp.global_q_amax(inp)
     q_scale = (qa / np.float32(127)).astype(np.float32)
     wq = qs.shape[2]
     assert np.array_equal(qs.view(np.uint32), q_scale[:, :, :wq].view(np.uint32))
-    row_qs = np.repeat(q_scale, 128, axis=2)[:, :, :S]                    # [B, H, S]
+    row_qs = np.repeat(q_scale, wl.q_group, axis=2)[:, :, :S]             # [B, H, S]
     assert np.array_equal(q8, hp.int8_codes(qf, row_qs.transpose(0, 2, 1)[..., None]))
 
     # K: live rows and live groups from the global group amax of live rows
@@ -69,12 +69,12 @@ def test_unpack_shapes_tail_and_scale_prefix(wl):
         assert v8.shape == (wl.B, wl.D, wl.h, Spad)
         assert not np.any(v8[..., S:])
         assert np.all(np.isfinite(qs)) and np.all(np.isfinite(ks))
-        wq, wk = O.scale_widths(S if wl.scale_sequence is None else wl.scale_sequence)
+        wq, wk = O.scale_widths(S if wl.scale_sequence is None else wl.scale_sequence, wl.q_group)
         assert qs.shape == (wl.B, wl.h, wq) and ks.shape == (wl.B, wl.h, wk)
         # scale_sequence narrows the scales to the leading slots of full width
         full = O.unpack_for_sage(np.ascontiguousarray(res["recv"][p]), batch_size=wl.B,
                                  local_sequence=wl.L, local_heads=wl.h, head_dim=wl.D,
-                                 world_size=wl.P, scale_sequence=None)
+                                 world_size=wl.P, scale_sequence=None, q_group=wl.q_group)
         assert np.array_equal(full[0], q8) and np.array_equal(full[1], k8)
         assert np.array_equal(full[2], v8)
         assert full[3][:, :, :wq].tobytes() == np.ascontiguousarray(qs).tobytes()
@@ -86,8 +86,9 @@ def test_shared_boundary_scale_bytes_agree(wl):
     """A group touched by two ranks carries the same scale bytes in both
     sources' chunks (group-wide identical values)."""
     inp, res = hp.cached(wl)
-    lay = O.chunk_layout(wl.B, wl.L, wl.h, wl.D)
-    for G, key, n in ((64, "k_scale", O.slots(wl.L, 64)), (128, "q_scale", O.slots(wl.L, 128))):
+    lay = O.chunk_layout(wl.B, wl.L, wl.h, wl.D, wl.q_group)
+    G_Q = wl.q_group
+    for G, key, n in ((64, "k_scale", O.slots(wl.L, 64)), (G_Q, "q_scale", O.slots(wl.L, G_Q))):
         for g in range((wl.S + G - 1) // G):
             rs = hp.ranks_touching(g, wl.L, wl.P, G)
             vals = []
@@ -102,14 +103,15 @@ def test_shared_boundary_scale_bytes_agree(wl):
                 assert v.tobytes() == per_rank[0].tobytes(), (key, g)
 
 
-@pytest.mark.parametrize("wl", [hp.TINY, hp.LONG_R, hp.HEAVY_R], ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", [hp.TINY, hp.LONG_R, hp.HEAVY_R, hp.G64[1]], ids=lambda w: w.name)
 def test_dequantisation_error_bounds(wl):
     """|code * scale - x| <= scale/2 (within a binary32 rounding) wherever
     the code did not saturate, and each group's amax element maps to +-127."""
     inp, res = hp.cached(wl)
     q8, k8, v8, qs, ks = _assemble(res, wl)
     qf = hp.f32(inp.q, wl.dtype).astype(np.float64)
-    row_qs = np.repeat(hp.global_q_amax(inp).astype(np.float64) / 127, 128, axis=2)[:, :, :wl.S]
+    row_qs = np.repeat(hp.global_q_amax(inp).astype(np.float64) / 127, wl.q_group,
+                       axis=2)[:, :, :wl.S]
     s = row_qs.transpose(0, 2, 1)[..., None]
     err = np.abs(q8.astype(np.float64) * s - qf)
     ok = np.abs(q8) < 127
