@@ -84,7 +84,7 @@ extern "C" {
 
 typedef void *ulp_stream_t; /* a cudaStream_t */
 
-enum { ULP_BF16 = 0, ULP_FP16 = 1 };
+enum { ULP_BF16 = 0, ULP_FP16 = 1, ULP_F32 = 2 /* attention output only */ };
 
 enum {
     ULP_OK = 0,
@@ -262,6 +262,36 @@ int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int D, int wor
                         int aligned, int scale_sequence, int q_group, int8_t *q8, int8_t *k8,
                         uint8_t *v8, float *q_scale, float *k_scale, int num_dests,
                         int enable_pdl, ulp_stream_t stream);
+
+/* Attention over the unpacked tensors of one destination -- the consumer the
+ * page "unpack_for_sage" hands its outputs to (INT8 Q/K, FP8 E4M3 V, FP32
+ * scales of width scale_widths(n) derived from the n rows attended over; "V
+ * scale remains with the caller and must be passed separately to
+ * attention").  The pages print no formula for it; this library's reading,
+ * non-causal softmax attention over the live prefix t, u < n:
+ *   Q[t] = q8[t] * q_scale[t / q_group], K[u] = k8[u] * k_scale[u / 64],
+ *   V[u, d] = e4m3(v8[d, u]) * v_scale[d],
+ *   O[b, t, j, :] = sum_u softmax_u(sm_scale * Q[t] . K[u]) V[u]
+ * (K centred by the mean attends the same: q . m is one constant per query).
+ * Computed on tensor cores with fp16 operands and fp32 accumulation: the
+ * integer logits are exact, P is rounded to fp16 (relative 2^-11) and the
+ * denominator sums the rounded values.
+ *   q8, k8    [B, S, h, D] int8 (rows >= n are not read)
+ *   v8        [B, D, h, Spad] E4M3 bytes, Spad = ceil(S/64)*64
+ *   q_scale   [B, h, ceil(n/q_group)] fp32; k_scale [B, h, ceil(n/64)] fp32
+ *   v_scale   [B, h, D] fp32: the caller's V scale of this destination's heads
+ *   out       [B, n, h, D] of out_dtype (ULP_F32, ULP_BF16 or ULP_FP16)
+ *   sm_scale  positive and finite (the usual choice is 1/sqrt(D))
+ *   status    NULL, or a device int that the kernel sets to a non-zero code
+ *             if a tensor-core product does not complete within about a
+ *             second (the kernel then frees its tensor memory and returns
+ *             without writing out); the caller clears it.
+ * D is 64 or 128, 1 <= n <= S; pointers as for the other calls (16-byte
+ * alignment for tensors, 4 bytes for the scales). */
+int ulp_sage_attention(const int8_t *q8, const int8_t *k8, const uint8_t *v8, const float *q_scale,
+                       const float *k_scale, const float *v_scale, int B, int S, int h, int D, int n,
+                       int q_group, float sm_scale, void *out, int out_dtype, int *status,
+                       ulp_stream_t stream);
 
 /* Message of the calling thread's last failed call ("" if none). */
 const char *ulp_last_error(void);

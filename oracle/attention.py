@@ -50,8 +50,9 @@ def dequantize(q8, k8, v8, q_scale, k_scale, v_scale, *, n: int, q_group: int = 
 
 
 def sage_attention(q8, k8, v8, q_scale, k_scale, v_scale, *, n: int, q_group: int = 128,
-                   sm_scale: float | None = None) -> np.ndarray:
-    """O [B, n, h, D] float64.
+                   sm_scale: float | None = None, rows=None) -> np.ndarray:
+    """O [B, n, h, D] float64 (or [B, len(rows), h, D] for the query rows
+    ``rows`` only, each row by the same definition).
 
     q8, k8: int8 [B, S, h, D]; v8: uint8 (E4M3 bytes) [B, D, h, Spad];
     q_scale: [B, h, >= ceil(n/q_group)], k_scale: [B, h, >= ceil(n/64)] fp32;
@@ -61,10 +62,12 @@ def sage_attention(q8, k8, v8, q_scale, k_scale, v_scale, *, n: int, q_group: in
     if sm_scale is None:
         sm_scale = 1.0 / np.sqrt(D)
     Q, K, V = dequantize(q8, k8, v8, q_scale, k_scale, v_scale, n=n, q_group=q_group)
-    O = np.empty((B, n, h, D), np.float64)
+    if rows is not None:
+        Q = Q[:, np.asarray(rows)]
+    O = np.empty((B, Q.shape[1], h, D), np.float64)
     for b in range(B):
         for j in range(h):
-            s = sm_scale * (Q[b, :, j] @ K[b, :, j].T)             # [n, n]
+            s = sm_scale * (Q[b, :, j] @ K[b, :, j].T)             # [queries, n]
             s -= s.max(axis=1, keepdims=True)
             p = np.exp(s)
             O[b, :, j] = (p @ V[b, :, j]) / p.sum(axis=1, keepdims=True)

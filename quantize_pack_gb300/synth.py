@@ -132,3 +132,45 @@ def make_inputs(wl: Workload) -> Inputs:
 
     return Inputs(wl=wl, q=qb, k=kb, v=vb, k_mean=np.ascontiguousarray(k_mean),
                   v_scale=np.ascontiguousarray(v_scale))
+
+
+@dataclasses.dataclass
+class AttentionOperands:
+    """Quantised operands of the attention consumer, as unpack_for_sage
+    returns them for one destination, plus the caller's V scale."""
+    q8: np.ndarray        # int8 [B, S, h, D]
+    k8: np.ndarray        # int8 [B, S, h, D]
+    v8: np.ndarray        # uint8 E4M3 bytes [B, D, h, Spad]
+    q_scale: np.ndarray   # fp32 [B, h, ceil(n / q_group)]
+    k_scale: np.ndarray   # fp32 [B, h, ceil(n / 64)]
+    v_scale: np.ndarray   # fp32 [B, h, D]
+    n: int
+    q_group: int
+
+
+def attention_operands(seed: int, *, B: int, S: int, h: int, D: int, n: Optional[int] = None,
+                       q_group: int = 128, spread: float = 1.0) -> AttentionOperands:
+    """Seeded random codes and scales (PCG64 ``default_rng(seed)``, draws in
+    this order): Q and K codes uniform in [-127, 127]; V bytes uniform over
+    the finite E4M3 codes (the NaN codes 0x7F/0xFF are replaced by 0x3C, and
+    the tail [S, Spad) is zero); Q and K scales uniform in
+    [0.5, 2] * spread / (127 * 8) per group; V scales uniform in
+    [0.01, 0.05] per channel.  ``spread`` widens the logits (peakier
+    softmax).  Rows [n, S) of Q and K and keys [n, S) of V get extreme codes
+    (+-127, 0x7E), which a consumer of the live prefix must ignore."""
+    rng = np.random.default_rng(seed)
+    n = S if n is None else n
+    Spad = (S + 63) // 64 * 64
+    q8 = rng.integers(-127, 128, size=(B, S, h, D), dtype=np.int8)
+    k8 = rng.integers(-127, 128, size=(B, S, h, D), dtype=np.int8)
+    v8 = rng.integers(0, 256, size=(B, D, h, Spad)).astype(np.uint8)
+    v8[(v8 & 0x7F) == 0x7F] = 0x3C
+    v8[..., S:] = 0
+    wq, wk = (n + q_group - 1) // q_group, (n + 63) // 64
+    qs = (spread * rng.uniform(0.5, 2.0, size=(B, h, wq)) / 127 / 8).astype(np.float32)
+    ks = (spread * rng.uniform(0.5, 2.0, size=(B, h, wk)) / 127 / 8).astype(np.float32)
+    vs = rng.uniform(0.01, 0.05, size=(B, h, D)).astype(np.float32)
+    q8[:, n:] = 127
+    k8[:, n:] = -127
+    v8[..., n:S] = 0x7E
+    return AttentionOperands(q8, k8, v8, qs, ks, vs, n, q_group)

@@ -22,7 +22,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libulp.so")
 
-ULP_BF16, ULP_FP16 = 0, 1
+ULP_BF16, ULP_FP16, ULP_F32 = 0, 1, 2
 ULP_ALL_RANKS = -1
 SEND_SOURCE_MAJOR, SEND_DEST_MAJOR = 0, 1
 GK, GQ = 64, 128   # K group rows; default Q group rows (q_group=64 selects the other width)
@@ -68,10 +68,13 @@ def lib() -> ctypes.CDLL:
         L.ulp_alltoall_emulate.argtypes = [_P, _P, _I, _SZ, _P]
         L.ulp_unpack_for_sage.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                                           _I, _I, _P]
+        L.ulp_sage_attention.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                         ctypes.c_float, _P, _I, _P, _P]
         for name in ("ulp_slots", "ulp_scale_widths", "ulp_chunk_bytes", "ulp_chunk_offsets",
                      "ulp_k_mean_workspace_bytes", "ulp_k_mean_global", "ulp_k_mean_global_noalloc",
                      "ulp_k_grouped_amax", "ulp_boundary_minmax", "ulp_derive_k_boundary_amax",
-                     "ulp_pack", "ulp_alltoall_emulate", "ulp_unpack_for_sage"):
+                     "ulp_pack", "ulp_alltoall_emulate", "ulp_unpack_for_sage",
+                     "ulp_sage_attention"):
             getattr(L, name).restype = _I
         _lib = L
     return _lib
@@ -319,3 +322,39 @@ def unpack_for_sage(recv_u8: torch.Tensor, *, batch_size: int, local_sequence: i
                                      1 if nd is None else nd, _pdl(enable_pdl),
                                      _stream(recv_u8.device)))
     return tuple(out)
+
+
+# ------------------------------------------------------------- the consumer
+
+_OUT_CODES = {torch.float32: ULP_F32, torch.bfloat16: ULP_BF16, torch.float16: ULP_FP16}
+
+
+def sage_attention(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale: torch.Tensor,
+                   k_scale: torch.Tensor, v_scale: torch.Tensor, *, n: Optional[int] = None,
+                   q_group: int = GQ, sm_scale: Optional[float] = None,
+                   out: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.bfloat16,
+                   status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Softmax attention over the unpacked tensors of one destination.
+
+    q8, k8 [B, S, h, D] int8; v8 [B, D, h, Spad] E4M3 bytes (uint8 or
+    float8_e4m3fn); q_scale [B, h, ceil(n/q_group)], k_scale [B, h,
+    ceil(n/64)] fp32 (unpack_for_sage with scale_sequence=n gives exactly
+    these); v_scale [B, h, D] fp32 (the caller's V scale of this
+    destination's heads).  Attends over the live prefix of n rows (default S)
+    and returns O [B, n, h, D] in out_dtype; sm_scale defaults to 1/sqrt(D).
+    ``status``: optional int32 device tensor of one element, set non-zero by
+    the kernel if a tensor-core product does not complete in time."""
+    B, S, h, D = q8.shape
+    n = S if n is None else int(n)
+    if sm_scale is None:
+        sm_scale = D ** -0.5
+    if out is None:
+        out = torch.empty((B, n, h, D), dtype=out_dtype, device=q8.device)
+    if out.dtype not in _OUT_CODES:
+        raise TypeError(f"out must be float32, bfloat16 or float16, got {out.dtype}")
+    v8b = v8.view(torch.uint8) if v8.dtype != torch.uint8 else v8
+    st = 0 if status is None else _ptr(status)
+    _check(lib().ulp_sage_attention(_ptr(q8), _ptr(k8), _ptr(v8b), _ptr(q_scale), _ptr(k_scale),
+                                    _ptr(v_scale), B, S, h, D, n, q_group, float(sm_scale),
+                                    _ptr(out), _OUT_CODES[out.dtype], st, _stream(q8.device)))
+    return out

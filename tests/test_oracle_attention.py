@@ -108,6 +108,14 @@ def test_against_torch_attention(q_group, B, S, h, D, n):
                        atol=1e-14)
 
 
+def test_selected_rows_equal_the_full_result():
+    c = make(12, S=300, h=2, D=64, n=280, q_group=64)
+    O = run(c)
+    rows = [0, 63, 64, 200, 279]
+    # the same values up to the library matmul's summation order
+    assert np.allclose(run(c, rows=rows), O[:, rows], rtol=1e-13, atol=1e-16)
+
+
 def test_zero_queries_average_the_values():
     c = make(3, S=200, h=2, D=64, n=190)
     c["q8"][:] = 0
