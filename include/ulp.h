@@ -275,7 +275,9 @@ int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int D, int wor
  * (K centred by the mean attends the same: q . m is one constant per query).
  * Computed on tensor cores with fp16 operands and fp32 accumulation: the
  * integer logits are exact, P is rounded to fp16 (relative 2^-11) and the
- * denominator sums the rounded values.
+ * denominator sums the rounded values.  A first kernel widens Q, K and V to
+ * fp16 in the workspace (at least ulp_sage_attention_workspace_bytes bytes;
+ * contents on return unspecified), the second runs the attention from it.
  *   q8, k8    [B, S, h, D] int8 (rows >= n are not read)
  *   v8        [B, D, h, Spad] E4M3 bytes, Spad = ceil(S/64)*64
  *   q_scale   [B, h, ceil(n/q_group)] fp32; k_scale [B, h, ceil(n/64)] fp32
@@ -290,8 +292,12 @@ int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int D, int wor
  * alignment for tensors, 4 bytes for the scales). */
 int ulp_sage_attention(const int8_t *q8, const int8_t *k8, const uint8_t *v8, const float *q_scale,
                        const float *k_scale, const float *v_scale, int B, int S, int h, int D, int n,
-                       int q_group, float sm_scale, void *out, int out_dtype, int *status,
-                       ulp_stream_t stream);
+                       int q_group, float sm_scale, void *workspace, size_t workspace_bytes,
+                       void *out, int out_dtype, int *status, ulp_stream_t stream);
+
+/* Workspace bytes ulp_sage_attention needs: 6 * B * h * ceil(n/128)*128 * D
+ * (Q, K, V in fp16 over the live prefix rounded up to 128 rows). */
+int ulp_sage_attention_workspace_bytes(int B, int S, int h, int D, int n, size_t *bytes);
 
 /* Message of the calling thread's last failed call ("" if none). */
 const char *ulp_last_error(void);

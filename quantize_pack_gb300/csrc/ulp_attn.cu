@@ -10,23 +10,31 @@
 // 128^3 = 2^21 the integer dot products accumulate exactly in fp32; E4M3 is a
 // subset of fp16, so V widens exactly too.  The per-group scales multiply the
 // integer logits in fp32.  P = exp2(x - m) is rounded to fp16 for the PV
-// product, and the softmax denominator sums the rounded values, so the
-// output is an exact weighted mean with weights perturbed by at most 2^-11
-// relative.
+// product and the softmax denominator sums the rounded values, so the output
+// is an exact weighted mean with weights perturbed by at most 2^-11 relative.
 //
-// One CTA of 128 threads per (b, head, 128-query tile); thread i owns query
-// row i (TMEM lane i).  Per 128-key tile:
-//   1. K (int8 -> fp16) and V (E4M3 -> fp16) tiles go to shared memory in
-//      the 128-byte swizzled K-major layout;
-//   2. one thread issues S = Q K^T (D/16 MMAs, M = N = 128) into TMEM;
-//   3. each thread reads its S row, applies the scales, updates its running
-//      max m and sum l (online softmax), writes its P row (fp16) to shared
-//      memory and rescales its O row in TMEM when m grew;
-//   4. one thread issues O += P V (8 MMAs, M = 128, N = D).
-// Every wait on an MMA completion is bounded; on timeout the kernel records
-// a status, frees its tensor memory and returns.
+// Two kernels.  The widen pass writes Q and K as fp16 [B*h, T, D] and V as
+// fp16 [B*h, D, T] (T = the live prefix rounded up to 128 rows, zero past
+// it) into a workspace, once per call, so the attention kernel moves every
+// tile with TMA straight into the tensor core's 128-byte swizzled operand
+// layout.  The attention kernel runs one CTA of six warps per (b, head,
+// 128-query tile):
+//   warp 4 (TMA): Q once, then K and V tiles of 128 keys into two stages;
+//   warp 5 (MMA, one thread): S_i = Q K_i^T into one of two TMEM buffers
+//     while the softmax warps work on S_{i-1}, then O += P_{i-1} V_{i-1};
+//   warps 0-3 (softmax, one query row per thread = TMEM lane): scale the
+//     integer logits, keep the running max m and sum l, write P (fp16) to
+//     shared memory.  m moves only when the tile's max exceeds it by more
+//     than 8 (log2 units), so O is rescaled rarely; weights stay <= 2^8 and
+//     numerator and denominator share the same m, so this is exact algebra.
+// Every mbarrier wait is bounded: on a timeout the CTA records a status,
+// every role stops, the tensor memory is freed and nothing is written.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
+
+#include <algorithm>
+#include <mutex>
 
 #include "ulp_internal.cuh"
 #include "ulp_tc.cuh"
@@ -35,44 +43,26 @@ namespace ulp {
 
 namespace {
 
-constexpr int kAttnThreads = 128;
 constexpr int kTile = 128;                 // queries per CTA, keys per step
-constexpr uint32_t kTmemCols = 256;        // S: 128 columns, O: D columns
+constexpr int kSoftmaxThreads = 128;       // warps 0-3
+constexpr int kAttnThreads = 192;          // + TMA warp + MMA warp
+constexpr uint32_t kTmemCols = 512;        // S0, S1: 128 columns each; O: D columns
 constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr float kRescaleLog2 = 8.0f;       // max growth (log2) absorbed without rescaling O
 
-struct AttnArgs {
-    const int8_t *q8, *k8;
-    const uint8_t *v8;
-    const float *qs, *ks, *vs;
-    void *out;
-    int *status;
-    int out_dtype;
-    int S, h, n, Spad, gq, wq, wk;
-    float scale_log2;                      // sm_scale * log2(e)
-};
-
-template <int D>
-struct AttnLayout {
-    static constexpr uint32_t q = 0;
-    static constexpr uint32_t k = q + kTile * D * 2;
-    static constexpr uint32_t v = k + kTile * D * 2;
-    static constexpr uint32_t p = v + D * kTile * 2;
-    static constexpr uint32_t bars = p + kTile * kTile * 2;   // bar_s, bar_o, tmem address, abort
-    static constexpr uint32_t bytes = bars + 64;
-};
+// ------------------------------------------------------------ widen pass
 
 // 4 int8 -> 4 fp16, exact: byte u = x + 128 becomes fp16 1024 + u (bits
 // 0x6400 | u), minus 1152.
 __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi)
 {
     const uint32_t u = w ^ 0x80808080u;
-    lo = __byte_perm(u, 0x64646464u, 0x5140);
-    hi = __byte_perm(u, 0x64646464u, 0x7362);
     const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-    __half2 a = __hsub2(*reinterpret_cast<__half2 *>(&lo), bias);
-    __half2 b = __hsub2(*reinterpret_cast<__half2 *>(&hi), bias);
-    lo = *reinterpret_cast<uint32_t *>(&a);
-    hi = *reinterpret_cast<uint32_t *>(&b);
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x5140), b = __byte_perm(u, 0x64646464u, 0x7362);
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t *>(&ha);
+    hi = *reinterpret_cast<const uint32_t *>(&hb);
 }
 
 // 2 E4M3 bytes (low 16 bits) -> fp16x2, exact.
@@ -82,64 +72,43 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16(uint32_t w)
     return (uint32_t)r.x | ((uint32_t)r.y << 16);
 }
 
-// 16 int8 codes -> two 16-byte fp16 chunks c0, c1 of row r in an R-row tile.
-__device__ __forceinline__ void store_i8_row16(uint8_t *tile, int r, int c0, int R, uint4 w)
-{
-    uint4 a, b;
-    i8x4_to_f16(w.x, a.x, a.y);
-    i8x4_to_f16(w.y, a.z, a.w);
-    i8x4_to_f16(w.z, b.x, b.y);
-    i8x4_to_f16(w.w, b.z, b.w);
-    *reinterpret_cast<uint4 *>(tile + tc::sw128_offset(r, c0, R)) = a;
-    *reinterpret_cast<uint4 *>(tile + tc::sw128_offset(r, c0 + 1, R)) = b;
-}
+struct WidenArgs {
+    const int8_t *q8, *k8;
+    const uint8_t *v8;
+    uint16_t *q16, *k16, *v16;             // [B*h, T, D], [B*h, T, D], [B*h, D, T]
+    int S, h, D, n, T, Spad;
+};
 
-__device__ __forceinline__ void store_e4m3_row16(uint8_t *tile, int r, int c0, int R, uint4 w)
+// blockIdx.z: 0 = Q, 1 = K, 2 = V; blockIdx.y = b * h + j; one thread per 16
+// input bytes (T * D / 16 chunks per head for each tensor).
+__global__ void __launch_bounds__(256) attn_widen_kernel(WidenArgs a)
 {
-    uint4 a, b;
-    a.x = e4m3x2_to_f16(w.x);
-    a.y = e4m3x2_to_f16(w.x >> 16);
-    a.z = e4m3x2_to_f16(w.y);
-    a.w = e4m3x2_to_f16(w.y >> 16);
-    b.x = e4m3x2_to_f16(w.z);
-    b.y = e4m3x2_to_f16(w.z >> 16);
-    b.z = e4m3x2_to_f16(w.w);
-    b.w = e4m3x2_to_f16(w.w >> 16);
-    *reinterpret_cast<uint4 *>(tile + tc::sw128_offset(r, c0, R)) = a;
-    *reinterpret_cast<uint4 *>(tile + tc::sw128_offset(r, c0 + 1, R)) = b;
-}
-
-// Rows [row0, row0 + 128) of an int8 [.., S, h, D] tensor (head j of batch
-// b) -> fp16 tile; rows >= n are zero.
-template <int D>
-__device__ __forceinline__ void load_i8_tile(uint8_t *tile, const int8_t *src, int row0, int n, int hD)
-{
-    constexpr int NV = D / 16;                 // 16-byte vectors per row
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-        const int idx = i * kAttnThreads + threadIdx.x;
-        const int r = idx / NV, cv = idx % NV;
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (row0 + r < n) w = *reinterpret_cast<const uint4 *>(src + (size_t)(row0 + r) * hD + cv * 16);
-        store_i8_row16(tile, r, 2 * cv, kTile, w);
-    }
-}
-
-// Keys [u0, u0 + 128) of every channel of V (E4M3 rows of Spad bytes, one per
-// channel d at src + d * ch_stride) -> fp16 tile of D rows; keys >= n are zero.
-template <int D>
-__device__ __forceinline__ void load_v_tile(uint8_t *tile, const uint8_t *src, size_t ch_stride, int u0, int n)
-{
-    constexpr int NV = kTile / 16;             // 16-byte vectors per channel row
-#pragma unroll
-    for (int i = 0; i < D * NV / kAttnThreads; ++i) {
-        const int idx = i * kAttnThreads + threadIdx.x;
-        const int d = idx / NV, cv = idx % NV;
-        const int key = u0 + cv * 16;
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (key < n) {
-            w = *reinterpret_cast<const uint4 *>(src + (size_t)d * ch_stride + key);
-            const int valid = n - key;         // bytes past it are zeroed
+    const int which = blockIdx.z, bh = blockIdx.y;
+    const int b = bh / a.h, j = bh - b * a.h;
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long per = (long long)a.T * a.D / 16;
+    if (idx >= per) return;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    uint4 lo, hi;
+    if (which < 2) {
+        const int nv = a.D / 16;
+        const int t = (int)(idx / nv), cv = (int)(idx % nv);
+        const int8_t *src = which == 0 ? a.q8 : a.k8;
+        if (t < a.n) w = *reinterpret_cast<const uint4 *>(src + (((size_t)b * a.S + t) * a.h + j) * a.D + cv * 16);
+        i8x4_to_f16(w.x, lo.x, lo.y);
+        i8x4_to_f16(w.y, lo.z, lo.w);
+        i8x4_to_f16(w.z, hi.x, hi.y);
+        i8x4_to_f16(w.w, hi.z, hi.w);
+        uint16_t *dst = (which == 0 ? a.q16 : a.k16) + ((size_t)bh * a.T + t) * a.D + cv * 16;
+        reinterpret_cast<uint4 *>(dst)[0] = lo;
+        reinterpret_cast<uint4 *>(dst)[1] = hi;
+    } else {
+        const int nv = a.T / 16;
+        const int d = (int)(idx / nv), cv = (int)(idx % nv);
+        const int key = cv * 16;
+        if (key < a.n) {
+            w = *reinterpret_cast<const uint4 *>(a.v8 + (((size_t)b * a.D + d) * a.h + j) * a.Spad + key);
+            const int valid = a.n - key;   // keys past the prefix become zero
             if (valid < 16) {
                 uint32_t *ww = reinterpret_cast<uint32_t *>(&w);
 #pragma unroll
@@ -149,12 +118,43 @@ __device__ __forceinline__ void load_v_tile(uint8_t *tile, const uint8_t *src, s
                 }
             }
         }
-        store_e4m3_row16(tile, d, 2 * cv, D, w);
+        lo = make_uint4(e4m3x2_to_f16(w.x), e4m3x2_to_f16(w.x >> 16), e4m3x2_to_f16(w.y), e4m3x2_to_f16(w.y >> 16));
+        hi = make_uint4(e4m3x2_to_f16(w.z), e4m3x2_to_f16(w.z >> 16), e4m3x2_to_f16(w.w), e4m3x2_to_f16(w.w >> 16));
+        uint16_t *dst = a.v16 + ((size_t)bh * a.D + d) * a.T + key;
+        reinterpret_cast<uint4 *>(dst)[0] = lo;
+        reinterpret_cast<uint4 *>(dst)[1] = hi;
     }
 }
 
+// ------------------------------------------------------- attention kernel
+
+struct AttnArgs {
+    const float *qs, *ks, *vs;
+    void *out;
+    int *status;
+    int out_dtype;
+    int h, n, gq, wq, wk, ntk;
+    float scale_log2;                      // sm_scale * log2(e)
+};
+
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 1) sage_attention_kernel(AttnArgs a)
+struct AttnLayout {
+    static constexpr uint32_t kBytes = kTile * D * 2;         // one Q or K tile
+    static constexpr uint32_t vBytes = D * kTile * 2;         // one V tile
+    static constexpr uint32_t q = 0;
+    static constexpr uint32_t k0 = q + kBytes;
+    static constexpr uint32_t v0 = k0 + 2 * kBytes;
+    static constexpr uint32_t p = v0 + 2 * vBytes;
+    static constexpr uint32_t bars = p + kTile * kTile * 2;
+    // q_full, kv_full[2], kv_empty[2], s_full[2], p_ready, o_done, then the
+    // TMEM address and the abort flag
+    static constexpr uint32_t bytes = bars + 16 * 8;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    sage_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, AttnArgs a)
 {
     using Lay = AttnLayout<D>;
     extern __shared__ uint8_t dyn_smem[];
@@ -162,180 +162,269 @@ __global__ void __launch_bounds__(kAttnThreads, 1) sage_attention_kernel(AttnArg
     // of the address)
     const uint32_t raw = tc::smem_u32(dyn_smem);
     uint8_t *sm = dyn_smem + ((1024u - (raw & 1023u)) & 1023u);
-    uint8_t *sq = sm + Lay::q, *sk = sm + Lay::k, *sv = sm + Lay::v, *sp = sm + Lay::p;
-    uint64_t *bar_s = reinterpret_cast<uint64_t *>(sm + Lay::bars);
-    uint64_t *bar_o = bar_s + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_s + 2);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::bars);
+    uint64_t *q_full = bars + 0, *kv_full = bars + 1, *kv_empty = bars + 3, *s_full = bars + 5;
+    uint64_t *p_ready = bars + 7, *o_done = bars + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9);
+    volatile int *abort = reinterpret_cast<volatile int *>(bars + 10);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.x * kTile, j = blockIdx.y, b = blockIdx.z;
-    const int hD = a.h * D;
-    const int n = a.n;
+    const int bh = b * a.h + j;
+    const int n = a.n, ntk = a.ntk;
 
-    if (warp == 0) tc::tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == 5) tc::tmem_alloc(tmem_slot, kTmemCols);
     if (tid == 0) {
-        tc::mbar_init(bar_s, 1);
-        tc::mbar_init(bar_o, 1);
+        tc::mbar_init(q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(kv_full + s, 1);
+            tc::mbar_init(kv_empty + s, 1);
+            tc::mbar_init(s_full + s, 1);
+        }
+        tc::mbar_init(p_ready, kSoftmaxThreads);
+        tc::mbar_init(o_done, 1);
+        *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // Q tile and this thread's Q scale
-    const int8_t *qsrc = a.q8 + (size_t)b * a.S * hD + (size_t)j * D;
-    const int8_t *ksrc = a.k8 + (size_t)b * a.S * hD + (size_t)j * D;
-    const uint8_t *vsrc = a.v8 + ((size_t)b * D * a.h + j) * a.Spad;
-    load_i8_tile<D>(sq, qsrc, t0, n, hD);
-    const int t = t0 + tid;
-    const float qa = t < n ? a.qs[((size_t)b * a.h + j) * a.wq + t / a.gq] * a.scale_log2 : 0.0f;
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tO = tmem + kTile;
-    const uint32_t lane_S = tc::tmem_addr(tS, warp * 32, 0), lane_O = tc::tmem_addr(tO, warp * 32, 0);
-    constexpr uint32_t idS = tc::idesc_f16_f32(kTile, kTile), idO = tc::idesc_f16_f32(kTile, D);
-    const uint32_t aq = tc::smem_u32(sq), ak = tc::smem_u32(sk), av = tc::smem_u32(sv), ap = tc::smem_u32(sp);
+    const uint32_t tS0 = tmem, tO = tmem + 2 * kTile;
 
-    float m_run = -INFINITY, l_run = 0.0f;
-    const int ntk = (n + kTile - 1) / kTile;
-    int fail_at = 0;                           // 1: S product, 2: PV product, 3: last PV product
-    uint64_t *fail_bar = bar_o;
-    uint32_t fail_par = 0;
-    for (int kt = 0; kt < ntk; ++kt) {
-        const int u0 = kt * kTile;
-        if (kt > 0) {                          // the previous PV product read V and P
-            const bool ok = tc::mbar_wait(bar_o, (kt - 1) & 1, kWaitNs);
-            if (__syncthreads_or(!ok)) { fail_at = 2; fail_bar = bar_o; fail_par = (kt - 1) & 1; break; }
-            tc::fence_after_sync();
-        }
-        load_i8_tile<D>(sk, ksrc, u0, n, hD);
-        load_v_tile<D>(sv, vsrc, (size_t)a.h * a.Spad, u0, n);
-        tc::fence_smem_to_async();
-        __syncthreads();
-        if (tid == 0) {
-            tc::fence_after_sync();
-#pragma unroll
-            for (int s = 0; s < D / 16; ++s)
-                tc::mma_f16(tS, tc::sw128_desc_k(aq, s, kTile), tc::sw128_desc_k(ak, s, kTile), idS, s > 0);
-            tc::mma_commit(bar_s);
-        }
-        // scales of the tile's two 64-key groups
-        const size_t krow = ((size_t)b * a.h + j) * a.wk;
-        const int g0 = u0 / 64;
-        const float c0 = qa * a.ks[krow + g0];
-        const float c1 = (g0 + 1 < a.wk) ? qa * a.ks[krow + g0 + 1] : 0.0f;
-        const int nvalid = min(kTile, n - u0);
-        {
-            const bool ok = tc::mbar_wait(bar_s, kt & 1, kWaitNs);
-            if (__syncthreads_or(!ok)) { fail_at = 1; fail_bar = bar_s; fail_par = kt & 1; break; }
-        }
-        tc::fence_after_sync();
-        float x[kTile];
-#pragma unroll
-        for (int cc = 0; cc < kTile / 32; ++cc) {
-            float v[32];
-            tc::tmem_ld32(lane_S + cc * 32, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[cc * 32 + i] = v[i];
-        }
-        float mt = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kTile; ++i) {
-            const float y = i < nvalid ? x[i] * (i < 64 ? c0 : c1) : -INFINITY;
-            x[i] = y;
-            mt = fmaxf(mt, y);
-        }
-        const float m_new = fmaxf(m_run, mt);
-        const float alpha = exp2f(m_run - m_new);   // 0 on the first tile
-        float lsum = 0.0f;
-#pragma unroll
-        for (int c = 0; c < kTile / 8; ++c) {
-            uint32_t w[4];
-#pragma unroll
-            for (int x2 = 0; x2 < 4; ++x2) {
-                const __half2 hp = __floats2half2_rn(exp2f(x[8 * c + 2 * x2] - m_new),
-                                                     exp2f(x[8 * c + 2 * x2 + 1] - m_new));
-                const float2 f = __half22float2(hp);
-                lsum += f.x + f.y;
-                w[x2] = *reinterpret_cast<const uint32_t *>(&hp);
+    if (warp == 4) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            tc::mbar_expect_tx(q_full, Lay::kBytes);
+            for (int kb = 0; kb < D / 64; ++kb)
+                tc::tma_load_3d(sm + Lay::q + kb * (kTile * 128), &tm_q, kb * 64, t0, bh, q_full);
+            int last[2] = {-1, -1};            // last tile loaded into each stage
+            for (int i = 0; i < ntk; ++i) {
+                const int s = i & 1;
+                if (i >= 2 && !tc::mbar_wait_abortable(kv_empty + s, ((i >> 1) - 1) & 1, kWaitNs, abort)) break;
+                tc::mbar_expect_tx(kv_full + s, Lay::kBytes + Lay::vBytes);
+                uint8_t *kd = sm + Lay::k0 + s * Lay::kBytes, *vd = sm + Lay::v0 + s * Lay::vBytes;
+                for (int kb = 0; kb < D / 64; ++kb)
+                    tc::tma_load_3d(kd + kb * (kTile * 128), &tm_k, kb * 64, i * kTile, bh, kv_full + s);
+                for (int c = 0; c < 2; ++c)
+                    tc::tma_load_3d(vd + c * (D * 128), &tm_v, i * kTile + c * 64, 0, bh, kv_full + s);
+                last[s] = i;
             }
-            *reinterpret_cast<uint4 *>(sp + tc::sw128_offset(tid, c, kTile)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        l_run = l_run * alpha + lsum;
-        m_run = m_new;
-        // O *= alpha for rows whose max grew (a warp-wide TMEM access)
-        if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                float v[32];
-                tc::tmem_ld32(lane_O + cc * 32, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                tc::tmem_st32(lane_O + cc * 32, v);
+            if (*abort) {                      // let the copies in flight land
+                tc::mbar_wait(q_full, 0, kWaitNs);
+                for (int s = 0; s < 2; ++s)
+                    if (last[s] >= 0) tc::mbar_wait(kv_full + s, (last[s] >> 1) & 1, kWaitNs);
             }
-            tc::tmem_st_wait();
         }
-        tc::fence_smem_to_async();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            tc::fence_after_sync();
+    } else if (warp == 5) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = tc::idesc_f16_f32(kTile, kTile), idO = tc::idesc_f16_f32(kTile, D);
+            const uint32_t aq = tc::smem_u32(sm + Lay::q), ap = tc::smem_u32(sm + Lay::p);
+            bool ok = tc::mbar_wait_abortable(q_full, 0, kWaitNs, abort);
+            for (int i = 0; ok && i <= ntk; ++i) {
+                if (i < ntk) {                 // S_i = Q K_i^T
+                    const int s = i & 1;
+                    if (!(ok = tc::mbar_wait_abortable(kv_full + s, (i >> 1) & 1, kWaitNs, abort))) break;
+                    tc::fence_after_sync();
+                    const uint32_t ak = tc::smem_u32(sm + Lay::k0 + s * Lay::kBytes);
 #pragma unroll
-            for (int s = 0; s < kTile / 16; ++s)
-                tc::mma_f16(tO, tc::sw128_desc_k(ap, s, kTile), tc::sw128_desc_k(av, s, D), idO,
-                            (kt > 0 || s > 0) ? 1u : 0u);
-            tc::mma_commit(bar_o);
-        }
-    }
-
-    if (fail_at == 0) {
-        const bool ok = tc::mbar_wait(bar_o, (ntk - 1) & 1, kWaitNs);
-        if (__syncthreads_or(!ok)) { fail_at = 3; fail_par = (ntk - 1) & 1; }
-    }
-    if (fail_at == 0) {
-        tc::fence_after_sync();
-        const float inv_l = 1.0f / l_run;
-        const float *vsc = a.vs + ((size_t)b * a.h + j) * D;
-        const size_t orow = (((size_t)b * n + t) * a.h + j) * D;
+                    for (int k = 0; k < D / 16; ++k)
+                        tc::mma_f16(tS0 + s * kTile, tc::sw128_desc_k(aq, k, kTile), tc::sw128_desc_k(ak, k, kTile),
+                                    idS, k > 0);
+                    tc::mma_commit(s_full + s);
+                }
+                if (i >= 1) {                  // O += P_{i-1} V_{i-1}
+                    const int pi = i - 1, s = pi & 1;
+                    if (!(ok = tc::mbar_wait_abortable(p_ready, pi & 1, kWaitNs, abort))) break;
+                    tc::fence_after_sync();
+                    const uint32_t av = tc::smem_u32(sm + Lay::v0 + s * Lay::vBytes);
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-            float v[32];
-            tc::tmem_ld32(lane_O + cc * 32, v);
-            if (t < n) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = v[i] * inv_l * vsc[cc * 32 + i];
-                if (a.out_dtype == ULP_F32) {
-                    float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + orow + cc * 32);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                } else {
-                    uint32_t w[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        if (a.out_dtype == ULP_BF16) {
-                            const __nv_bfloat162 hv = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-                            w[i] = *reinterpret_cast<const uint32_t *>(&hv);
-                        } else {
-                            const __half2 hv = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
-                            w[i] = *reinterpret_cast<const uint32_t *>(&hv);
-                        }
-                    }
-                    uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.out) + orow + cc * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) o[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    for (int k = 0; k < kTile / 16; ++k)
+                        tc::mma_f16(tO, tc::sw128_desc_k(ap, k, kTile), tc::sw128_desc_k(av, k, D), idO,
+                                    (pi > 0 || k > 0) ? 1u : 0u);
+                    tc::mma_commit(o_done);
+                    tc::mma_commit(kv_empty + s);
                 }
             }
         }
     } else {
-        // an MMA did not complete in time: report, give it a second bounded
-        // wait, then release the tensor memory
-        if (tid == 0 && a.status) atomicExch(a.status, fail_at);
-        tc::mbar_wait(fail_bar, fail_par, kWaitNs);
+        // ---------------------------------------------------------- softmax
+        const int t = t0 + tid;
+        const float qa = t < n ? a.qs[(size_t)bh * a.wq + t / a.gq] * a.scale_log2 : 0.0f;
+        const float *ksr = a.ks + (size_t)bh * a.wk;
+        uint8_t *prow = sm + Lay::p;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        float m_use = -INFINITY, l_run = 0.0f;
+        bool ok = true;
+        // a warp-uniform outcome, so the warp-wide TMEM accesses stay converged
+        auto wait_warp = [&](uint64_t *bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, tc::mbar_wait_abortable(bar, parity, kWaitNs, abort)) != 0;
+        };
+        for (int i = 0; i < ntk; ++i) {
+            const int u0 = i * kTile, sb = i & 1;
+            const float c0 = qa * ksr[u0 / 64];
+            const float c1 = (u0 / 64 + 1 < a.wk) ? qa * ksr[u0 / 64 + 1] : 0.0f;
+            if (!(ok = wait_warp(s_full + sb, (i >> 1) & 1))) break;
+            tc::fence_after_sync();
+            float x[kTile];
+#pragma unroll
+            for (int cc = 0; cc < kTile / 32; ++cc) {
+                float v[32];
+                tc::tmem_ld32(tS0 + sb * kTile + lane_base + cc * 32, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[cc * 32 + e] = v[e];
+            }
+            float mt = -INFINITY;
+            if (u0 + kTile <= n) {
+#pragma unroll
+                for (int e = 0; e < kTile; ++e) {
+                    x[e] *= e < 64 ? c0 : c1;
+                    mt = fmaxf(mt, x[e]);
+                }
+            } else {
+                const int nvalid = n - u0;
+#pragma unroll
+                for (int e = 0; e < kTile; ++e) {
+                    x[e] = e < nvalid ? x[e] * (e < 64 ? c0 : c1) : -INFINITY;
+                    mt = fmaxf(mt, x[e]);
+                }
+            }
+            const bool grow = mt > m_use + kRescaleLog2;   // always on the first tile
+            float alpha = 1.0f;
+            if (grow) {
+                alpha = exp2f(m_use - mt);                 // 0 on the first tile
+                m_use = mt;
+            }
+            uint32_t pk[kTile / 2];
+            float lsum = 0.0f;
+#pragma unroll
+            for (int e = 0; e < kTile / 2; ++e) {
+                const __half2 hp = __floats2half2_rn(exp2f(x[2 * e] - m_use), exp2f(x[2 * e + 1] - m_use));
+                const float2 f = __half22float2(hp);
+                lsum += f.x + f.y;
+                pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
+            }
+            l_run = l_run * alpha + lsum;
+            // P and O are free once the previous PV product completed
+            if (i >= 1) {
+                if (!(ok = wait_warp(o_done, (i - 1) & 1))) break;
+                tc::fence_after_sync();
+                if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        float v[32];
+                        tc::tmem_ld32(tO + lane_base + cc * 32, v);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] *= alpha;
+                        tc::tmem_st32(tO + lane_base + cc * 32, v);
+                    }
+                    tc::tmem_st_wait();
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < kTile / 8; ++c)
+                *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(tid, c, kTile)) =
+                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            tc::fence_smem_to_async();
+            tc::fence_before_sync();
+            tc::mbar_arrive(p_ready);
+        }
+        if (ok && wait_warp(o_done, (ntk - 1) & 1)) {
+            tc::fence_after_sync();
+            const float inv_l = 1.0f / l_run;
+            const float *vsc = a.vs + (size_t)bh * D;
+            const size_t orow = (((size_t)b * n + t) * a.h + j) * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                float v[32];
+                tc::tmem_ld32(tO + lane_base + cc * 32, v);
+                if (t < n) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = v[e] * inv_l * vsc[cc * 32 + e];
+                    if (a.out_dtype == ULP_F32) {
+                        float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + orow + cc * 32);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                    } else {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            if (a.out_dtype == ULP_BF16) {
+                                const __nv_bfloat162 hv = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+                                w[e] = *reinterpret_cast<const uint32_t *>(&hv);
+                            } else {
+                                const __half2 hv = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
+                                w[e] = *reinterpret_cast<const uint32_t *>(&hv);
+                            }
+                        }
+                        uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.out) + orow + cc * 32);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) o[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                    }
+                }
+            }
+        }
     }
+
+    // every role is done (or gave up); the CTA's tensor-core work has
+    // completed unless a wait timed out, in which case the last products get
+    // one more bounded wait before the tensor memory is released
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) {
+    if (*abort) {
+        if (tid == 0 && a.status) atomicExch(a.status, 1);
+        if (tid == 0) tc::mbar_wait(o_done, (ntk - 1) & 1, kWaitNs);
+        __syncthreads();
+    }
+    if (warp == 5) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// ------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// fp16 tensor [planes, rows, cols] (cols contiguous) as a 3-D map with
+// boxes of 64 columns x box_rows rows and the 128-byte swizzle.
+int make_map(CUtensorMap *m, void *base, uint64_t cols, uint64_t rows, uint64_t planes, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return fail(ULP_ECUDA, "sage_attention: cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[3] = {cols, rows, planes};
+    const cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+    const cuuint32_t box[3] = {64, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ULP_ECUDA, "sage_attention: tensor map encoding failed (%d)", (int)r);
+    return ULP_OK;
+}
+
+size_t widened_bytes(int B, int h, int D, int n)
+{
+    const size_t T = (size_t)(n + kTile - 1) / kTile * kTile;
+    return 3 * (size_t)B * h * T * D * 2;
 }
 
 }  // namespace
@@ -344,43 +433,73 @@ __global__ void __launch_bounds__(kAttnThreads, 1) sage_attention_kernel(AttnArg
 
 using namespace ulp;
 
+extern "C" int ulp_sage_attention_workspace_bytes(int B, int S, int h, int D, int n, size_t *bytes)
+{
+    if (B < 1 || S < 1 || h < 1 || (D != 64 && D != 128) || n < 1 || n > S || !bytes)
+        return fail(ULP_EINVAL, "sage_attention_workspace_bytes: bad sizes");
+    *bytes = widened_bytes(B, h, D, n);
+    return ULP_OK;
+}
+
 extern "C" int ulp_sage_attention(const int8_t *q8, const int8_t *k8, const uint8_t *v8, const float *q_scale,
                                   const float *k_scale, const float *v_scale, int B, int S, int h, int D,
-                                  int n, int q_group, float sm_scale, void *out, int out_dtype, int *status,
-                                  ulp_stream_t stream)
+                                  int n, int q_group, float sm_scale, void *workspace, size_t workspace_bytes,
+                                  void *out, int out_dtype, int *status, ulp_stream_t stream)
 {
     if (B < 1 || S < 1 || h < 1) return fail(ULP_EINVAL, "sage_attention: B, S, h must be positive");
     if (D != 64 && D != 128) return fail(ULP_EINVAL, "sage_attention: head_dim must be 64 or 128 (got %d)", D);
     if (n < 1 || n > S) return fail(ULP_EINVAL, "sage_attention: n = %d outside [1, %d]", n, S);
     if (int s = check_q_group(q_group, "sage_attention")) return s;
     if (out_dtype != ULP_F32 && out_dtype != ULP_BF16 && out_dtype != ULP_FP16)
-        return fail(ULP_EDTYPE, "sage_attention: out_dtype must be ULP_F32, ULP_BF16 or ULP_FP16 (got %d)", out_dtype);
+        return fail(ULP_EDTYPE, "sage_attention: out_dtype must be ULP_F32, ULP_BF16 or ULP_FP16 (got %d)",
+                    out_dtype);
     if (!(sm_scale > 0.0f) || !(sm_scale < INFINITY))
         return fail(ULP_EINVAL, "sage_attention: sm_scale must be positive and finite");
-    if ((long long)B * S * h * D > (1ll << 40)) return fail(ULP_EINVAL, "sage_attention: tensors too large");
-    if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(out) || !aligned4(q_scale) ||
-        !aligned4(k_scale) || !aligned4(v_scale))
-        return fail(ULP_EALIGN, "sage_attention: q8, k8, v8, out must be 16-byte aligned, scales 4-byte aligned");
+    if ((long long)B * S * h * D > (1ll << 40) || (long long)B * h > 65535)
+        return fail(ULP_EINVAL, "sage_attention: tensors too large");
+    if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(out) || !aligned16(workspace) ||
+        !aligned4(q_scale) || !aligned4(k_scale) || !aligned4(v_scale))
+        return fail(ULP_EALIGN, "sage_attention: q8, k8, v8, out, workspace must be 16-byte aligned, "
+                                "scales 4-byte aligned");
+    const size_t need = widened_bytes(B, h, D, n);
+    if (workspace_bytes < need)
+        return fail(ULP_EINVAL, "sage_attention: workspace of %zu bytes, %zu needed", workspace_bytes, need);
+    const int T = (n + kTile - 1) / kTile * kTile;
+    const int Spad = (S + 63) / 64 * 64;
+    const size_t plane = (size_t)B * h * T * D;
+    uint16_t *q16 = reinterpret_cast<uint16_t *>(workspace), *k16 = q16 + plane, *v16 = k16 + plane;
+
+    CUtensorMap mq, mk, mv;
+    if (int s = make_map(&mq, q16, D, T, (uint64_t)B * h, kTile)) return s;
+    if (int s = make_map(&mk, k16, D, T, (uint64_t)B * h, kTile)) return s;
+    if (int s = make_map(&mv, v16, T, D, (uint64_t)B * h, D)) return s;
+
+    const cudaStream_t st = (cudaStream_t)stream;
+    WidenArgs w{q8, k8, v8, q16, k16, v16, S, h, D, n, T, Spad};
+    const long long chunks = (long long)T * D / 16;
+    const dim3 wgrid((unsigned)((chunks + 255) / 256), (unsigned)(B * h), 3);
+    attn_widen_kernel<<<wgrid, 256, 0, st>>>(w);
+    if (int s = check_launch("sage_attention (widen)")) return s;
+
     AttnArgs a{};
-    a.q8 = q8; a.k8 = k8; a.v8 = v8;
     a.qs = q_scale; a.ks = k_scale; a.vs = v_scale;
     a.out = out; a.status = status; a.out_dtype = out_dtype;
-    a.S = S; a.h = h; a.n = n; a.Spad = (S + 63) / 64 * 64; a.gq = q_group;
+    a.h = h; a.n = n; a.gq = q_group;
     a.wq = (n + q_group - 1) / q_group;
     a.wk = (n + kGK - 1) / kGK;
+    a.ntk = T / kTile;
     a.scale_log2 = sm_scale * 1.4426950408889634f;
-    const int ntq = (n + kTile - 1) / kTile;
-    if (ntq > INT_MAX || h > 65535 || B > 65535) return fail(ULP_EINVAL, "sage_attention: grid too large");
-    const dim3 grid((unsigned)ntq, (unsigned)h, (unsigned)B);
-    const cudaStream_t st = (cudaStream_t)stream;
+    const dim3 grid((unsigned)a.ntk, (unsigned)h, (unsigned)B);
+    // one CTA per SM (it holds all 512 TMEM columns): at D = 64 the request
+    // is padded past half of the SM's shared memory
     if (D == 128) {
         const size_t bytes = AttnLayout<128>::bytes + 1024;
         cudaFuncSetAttribute(sage_attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-        sage_attention_kernel<128><<<grid, kAttnThreads, bytes, st>>>(a);
+        sage_attention_kernel<128><<<grid, kAttnThreads, bytes, st>>>(mq, mk, mv, a);
     } else {
-        const size_t bytes = AttnLayout<64>::bytes + 1024;
+        const size_t bytes = std::max<size_t>(AttnLayout<64>::bytes + 1024, 120 * 1024);
         cudaFuncSetAttribute(sage_attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-        sage_attention_kernel<64><<<grid, kAttnThreads, bytes, st>>>(a);
+        sage_attention_kernel<64><<<grid, kAttnThreads, bytes, st>>>(mq, mk, mv, a);
     }
     return check_launch("sage_attention");
 }

@@ -69,12 +69,13 @@ def lib() -> ctypes.CDLL:
         L.ulp_unpack_for_sage.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                                           _I, _I, _P]
         L.ulp_sage_attention.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
-                                         ctypes.c_float, _P, _I, _P, _P]
+                                         ctypes.c_float, _P, _SZ, _P, _I, _P, _P]
+        L.ulp_sage_attention_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]
         for name in ("ulp_slots", "ulp_scale_widths", "ulp_chunk_bytes", "ulp_chunk_offsets",
                      "ulp_k_mean_workspace_bytes", "ulp_k_mean_global", "ulp_k_mean_global_noalloc",
                      "ulp_k_grouped_amax", "ulp_boundary_minmax", "ulp_derive_k_boundary_amax",
                      "ulp_pack", "ulp_alltoall_emulate", "ulp_unpack_for_sage",
-                     "ulp_sage_attention"):
+                     "ulp_sage_attention", "ulp_sage_attention_workspace_bytes"):
             getattr(L, name).restype = _I
         _lib = L
     return _lib
@@ -333,6 +334,7 @@ def sage_attention(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale
                    k_scale: torch.Tensor, v_scale: torch.Tensor, *, n: Optional[int] = None,
                    q_group: int = GQ, sm_scale: Optional[float] = None,
                    out: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.bfloat16,
+                   workspace: Optional[torch.Tensor] = None,
                    status: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Softmax attention over the unpacked tensors of one destination.
 
@@ -342,6 +344,8 @@ def sage_attention(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale
     these); v_scale [B, h, D] fp32 (the caller's V scale of this
     destination's heads).  Attends over the live prefix of n rows (default S)
     and returns O [B, n, h, D] in out_dtype; sm_scale defaults to 1/sqrt(D).
+    ``workspace``: optional uint8 device buffer of at least
+    sage_attention_workspace_bytes(...) bytes (allocated when None).
     ``status``: optional int32 device tensor of one element, set non-zero by
     the kernel if a tensor-core product does not complete in time."""
     B, S, h, D = q8.shape
@@ -353,8 +357,18 @@ def sage_attention(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale
     if out.dtype not in _OUT_CODES:
         raise TypeError(f"out must be float32, bfloat16 or float16, got {out.dtype}")
     v8b = v8.view(torch.uint8) if v8.dtype != torch.uint8 else v8
+    if workspace is None:
+        workspace = torch.empty(sage_attention_workspace_bytes(B, S, h, D, n), dtype=torch.uint8,
+                                device=q8.device)
     st = 0 if status is None else _ptr(status)
     _check(lib().ulp_sage_attention(_ptr(q8), _ptr(k8), _ptr(v8b), _ptr(q_scale), _ptr(k_scale),
                                     _ptr(v_scale), B, S, h, D, n, q_group, float(sm_scale),
+                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                     _ptr(out), _OUT_CODES[out.dtype], st, _stream(q8.device)))
     return out
+
+
+def sage_attention_workspace_bytes(B: int, S: int, h: int, D: int, n: int) -> int:
+    nb = _SZ()
+    _check(lib().ulp_sage_attention_workspace_bytes(B, S, h, D, n, ctypes.byref(nb)))
+    return nb.value
