@@ -10,8 +10,9 @@
 // 128^3 = 2^21 the integer dot products accumulate exactly in fp32; E4M3 is a
 // subset of fp16, so V widens exactly too.  The per-group scales multiply the
 // integer logits in fp32.  P = exp2(x - m) is rounded to fp16 for the PV
-// product and the softmax denominator sums the rounded values, so the output
-// is an exact weighted mean with weights perturbed by at most 2^-11 relative.
+// product and the softmax denominator sums the same rounded values, so the
+// output is an exact weighted mean with weights perturbed by at most 2^-11
+// relative.  Scales must be positive (they are amax / 127).
 //
 // Two kernels.  The widen pass writes Q and K as fp16 [B*h, T, D] and V as
 // fp16 [B*h, D, T] (T = the live prefix rounded up to 128 rows, zero past
@@ -19,14 +20,17 @@
 // tile with TMA straight into the tensor core's 128-byte swizzled operand
 // layout.  The attention kernel runs one CTA of six warps per (b, head,
 // 128-query tile):
-//   warp 4 (TMA): Q once, then K and V tiles of 128 keys into two stages;
+//   warp 4 (TMA): Q once, then K and V tiles of 128 keys, two stages each (a
+//     K stage frees when its S product completes, a V stage after PV);
 //   warp 5 (MMA, one thread): S_i = Q K_i^T into one of two TMEM buffers
 //     while the softmax warps work on S_{i-1}, then O += P_{i-1} V_{i-1};
-//   warps 0-3 (softmax, one query row per thread = TMEM lane): scale the
-//     integer logits, keep the running max m and sum l, write P (fp16) to
+//   warps 0-3 (softmax, one query row per thread = TMEM lane): keep the
+//     running max m of the scaled logits, write P = 2^(S c - m) (fp16) to
 //     shared memory.  m moves only when the tile's max exceeds it by more
 //     than 8 (log2 units), so O is rescaled rarely; weights stay <= 2^8 and
 //     numerator and denominator share the same m, so this is exact algebra.
+//     The denominator is accumulated by the tensor core itself: each V tile
+//     carries a row of ones, so O's column D is the sum of the weights.
 // Every mbarrier wait is bounded: on a timeout the CTA records a status,
 // every role stops, the tensor memory is freed and nothing is written.
 #include <cuda.h>
@@ -46,9 +50,16 @@ namespace {
 constexpr int kTile = 128;                 // queries per CTA, keys per step
 constexpr int kSoftmaxThreads = 128;       // warps 0-3
 constexpr int kAttnThreads = 192;          // + TMA warp + MMA warp
-constexpr uint32_t kTmemCols = 512;        // S0, S1: 128 columns each; O: D columns
+constexpr uint32_t kTmemCols = 512;        // S0, S1: 128 columns each; O: D + 16 (sum in column D)
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr float kRescaleLog2 = 8.0f;       // max growth (log2) absorbed without rescaling O
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // ------------------------------------------------------------ widen pass
 
@@ -137,17 +148,21 @@ struct AttnArgs {
     float scale_log2;                      // sm_scale * log2(e)
 };
 
+// A V tile holds D channel rows and 16 more: a row of ones (so the PV product
+// also accumulates the softmax denominator, in O's column D) and 15 zero rows.
 template <int D>
 struct AttnLayout {
+    static constexpr int vRows = D + 16;
     static constexpr uint32_t kBytes = kTile * D * 2;         // one Q or K tile
-    static constexpr uint32_t vBytes = D * kTile * 2;         // one V tile
+    static constexpr uint32_t vBytes = vRows * kTile * 2;     // one V tile
+    static constexpr uint32_t vLoadBytes = D * kTile * 2;     // what TMA writes of it
     static constexpr uint32_t q = 0;
     static constexpr uint32_t k0 = q + kBytes;
     static constexpr uint32_t v0 = k0 + 2 * kBytes;
     static constexpr uint32_t p = v0 + 2 * vBytes;
     static constexpr uint32_t bars = p + kTile * kTile * 2;
-    // q_full, kv_full[2], kv_empty[2], s_full[2], p_ready, o_done, then the
-    // TMEM address and the abort flag
+    // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
+    // p_ready, o_done, then the TMEM address and the abort flag
     static constexpr uint32_t bytes = bars + 16 * 8;
 };
 
@@ -163,10 +178,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t raw = tc::smem_u32(dyn_smem);
     uint8_t *sm = dyn_smem + ((1024u - (raw & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::bars);
-    uint64_t *q_full = bars + 0, *kv_full = bars + 1, *kv_empty = bars + 3, *s_full = bars + 5;
-    uint64_t *p_ready = bars + 7, *o_done = bars + 8;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9);
-    volatile int *abort = reinterpret_cast<volatile int *>(bars + 10);
+    uint64_t *q_full = bars + 0, *k_full = bars + 1, *k_empty = bars + 3, *v_full = bars + 5, *v_empty = bars + 7;
+    uint64_t *s_full = bars + 9, *p_ready = bars + 11, *o_done = bars + 12;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
+    volatile int *abort = reinterpret_cast<volatile int *>(bars + 14);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.x * kTile, j = blockIdx.y, b = blockIdx.z;
@@ -174,11 +189,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int n = a.n, ntk = a.ntk;
 
     if (warp == 5) tc::tmem_alloc(tmem_slot, kTmemCols);
+    // the constant rows of both V stages (TMA writes only the first D rows of
+    // each 64-key block): row D = 1.0, rows D+1 .. D+15 = 0
+    for (int x = tid; x < 4 * 16 * 8; x += kAttnThreads) {
+        const int blk = x / 128, r = (x / 8) % 16, c = x % 8;
+        uint8_t *row = sm + Lay::v0 + (blk >> 1) * Lay::vBytes + (blk & 1) * (Lay::vRows * 128) + (D + r) * 128;
+        const uint32_t one2 = 0x3C003C00u;   // two fp16 ones
+        reinterpret_cast<uint4 *>(row)[c] = r == 0 ? make_uint4(one2, one2, one2, one2) : make_uint4(0, 0, 0, 0);
+    }
+    tc::fence_smem_to_async();
     if (tid == 0) {
         tc::mbar_init(q_full, 1);
         for (int s = 0; s < 2; ++s) {
-            tc::mbar_init(kv_full + s, 1);
-            tc::mbar_init(kv_empty + s, 1);
+            tc::mbar_init(k_full + s, 1);
+            tc::mbar_init(k_empty + s, 1);
+            tc::mbar_init(v_full + s, 1);
+            tc::mbar_init(v_empty + s, 1);
             tc::mbar_init(s_full + s, 1);
         }
         tc::mbar_init(p_ready, kSoftmaxThreads);
@@ -198,34 +224,41 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc::mbar_expect_tx(q_full, Lay::kBytes);
             for (int kb = 0; kb < D / 64; ++kb)
                 tc::tma_load_3d(sm + Lay::q + kb * (kTile * 128), &tm_q, kb * 64, t0, bh, q_full);
-            int last[2] = {-1, -1};            // last tile loaded into each stage
+            // K stages free up when S = Q K^T completes, V stages when PV
+            // does, so K runs ahead of V
+            int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};   // last tile loaded into each stage
             for (int i = 0; i < ntk; ++i) {
                 const int s = i & 1;
-                if (i >= 2 && !tc::mbar_wait_abortable(kv_empty + s, ((i >> 1) - 1) & 1, kWaitNs, abort)) break;
-                tc::mbar_expect_tx(kv_full + s, Lay::kBytes + Lay::vBytes);
+                if (i >= 2 && !tc::mbar_wait_abortable(k_empty + s, ((i >> 1) - 1) & 1, kWaitNs, abort)) break;
+                tc::mbar_expect_tx(k_full + s, Lay::kBytes);
                 uint8_t *kd = sm + Lay::k0 + s * Lay::kBytes, *vd = sm + Lay::v0 + s * Lay::vBytes;
                 for (int kb = 0; kb < D / 64; ++kb)
-                    tc::tma_load_3d(kd + kb * (kTile * 128), &tm_k, kb * 64, i * kTile, bh, kv_full + s);
+                    tc::tma_load_3d(kd + kb * (kTile * 128), &tm_k, kb * 64, i * kTile, bh, k_full + s);
+                last_k[s] = i;
+                if (i >= 2 && !tc::mbar_wait_abortable(v_empty + s, ((i >> 1) - 1) & 1, kWaitNs, abort)) break;
+                tc::mbar_expect_tx(v_full + s, Lay::vLoadBytes);
                 for (int c = 0; c < 2; ++c)
-                    tc::tma_load_3d(vd + c * (D * 128), &tm_v, i * kTile + c * 64, 0, bh, kv_full + s);
-                last[s] = i;
+                    tc::tma_load_3d(vd + c * (Lay::vRows * 128), &tm_v, i * kTile + c * 64, 0, bh, v_full + s);
+                last_v[s] = i;
             }
             if (*abort) {                      // let the copies in flight land
                 tc::mbar_wait(q_full, 0, kWaitNs);
-                for (int s = 0; s < 2; ++s)
-                    if (last[s] >= 0) tc::mbar_wait(kv_full + s, (last[s] >> 1) & 1, kWaitNs);
+                for (int s = 0; s < 2; ++s) {
+                    if (last_k[s] >= 0) tc::mbar_wait(k_full + s, (last_k[s] >> 1) & 1, kWaitNs);
+                    if (last_v[s] >= 0) tc::mbar_wait(v_full + s, (last_v[s] >> 1) & 1, kWaitNs);
+                }
             }
         }
     } else if (warp == 5) {
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idS = tc::idesc_f16_f32(kTile, kTile), idO = tc::idesc_f16_f32(kTile, D);
+            constexpr uint32_t idS = tc::idesc_f16_f32(kTile, kTile), idO = tc::idesc_f16_f32(kTile, Lay::vRows);
             const uint32_t aq = tc::smem_u32(sm + Lay::q), ap = tc::smem_u32(sm + Lay::p);
             bool ok = tc::mbar_wait_abortable(q_full, 0, kWaitNs, abort);
             for (int i = 0; ok && i <= ntk; ++i) {
                 if (i < ntk) {                 // S_i = Q K_i^T
                     const int s = i & 1;
-                    if (!(ok = tc::mbar_wait_abortable(kv_full + s, (i >> 1) & 1, kWaitNs, abort))) break;
+                    if (!(ok = tc::mbar_wait_abortable(k_full + s, (i >> 1) & 1, kWaitNs, abort))) break;
                     tc::fence_after_sync();
                     const uint32_t ak = tc::smem_u32(sm + Lay::k0 + s * Lay::kBytes);
 #pragma unroll
@@ -233,18 +266,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         tc::mma_f16(tS0 + s * kTile, tc::sw128_desc_k(aq, k, kTile), tc::sw128_desc_k(ak, k, kTile),
                                     idS, k > 0);
                     tc::mma_commit(s_full + s);
+                    tc::mma_commit(k_empty + s);
                 }
                 if (i >= 1) {                  // O += P_{i-1} V_{i-1}
                     const int pi = i - 1, s = pi & 1;
                     if (!(ok = tc::mbar_wait_abortable(p_ready, pi & 1, kWaitNs, abort))) break;
+                    if (!(ok = tc::mbar_wait_abortable(v_full + s, (pi >> 1) & 1, kWaitNs, abort))) break;
                     tc::fence_after_sync();
                     const uint32_t av = tc::smem_u32(sm + Lay::v0 + s * Lay::vBytes);
 #pragma unroll
                     for (int k = 0; k < kTile / 16; ++k)
-                        tc::mma_f16(tO, tc::sw128_desc_k(ap, k, kTile), tc::sw128_desc_k(av, k, D), idO,
+                        tc::mma_f16(tO, tc::sw128_desc_k(ap, k, kTile), tc::sw128_desc_k(av, k, Lay::vRows), idO,
                                     (pi > 0 || k > 0) ? 1u : 0u);
                     tc::mma_commit(o_done);
-                    tc::mma_commit(kv_empty + s);
+                    tc::mma_commit(v_empty + s);
                 }
             }
         }
@@ -255,7 +290,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const float *ksr = a.ks + (size_t)bh * a.wk;
         uint8_t *prow = sm + Lay::p;
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        float m_use = -INFINITY, l_run = 0.0f;
+        constexpr int OC = (D + 32) / 32;      // 32-column chunks of O, the sum column included
+        float m_use = -INFINITY;
         bool ok = true;
         // a warp-uniform outcome, so the warp-wide TMEM accesses stay converged
         auto wait_warp = [&](uint64_t *bar, uint32_t parity) {
@@ -275,44 +311,55 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) x[cc * 32 + e] = v[e];
             }
-            float mt = -INFINITY;
-            if (u0 + kTile <= n) {
+            // x holds the integer logits; the scales c0, c1 (>= 0) of the two
+            // 64-key groups are monotone, so the tile max is c * (max of the
+            // raw logits) and each weight is 2^fma(S, c, -m)
+            const int nvalid = min(kTile, n - u0);
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+            if (nvalid == kTile) {
 #pragma unroll
-                for (int e = 0; e < kTile; ++e) {
-                    x[e] *= e < 64 ? c0 : c1;
-                    mt = fmaxf(mt, x[e]);
-                }
+                for (int e = 0; e < 64; ++e) mx0 = fmaxf(mx0, x[e]);
+#pragma unroll
+                for (int e = 64; e < kTile; ++e) mx1 = fmaxf(mx1, x[e]);
             } else {
-                const int nvalid = n - u0;
 #pragma unroll
-                for (int e = 0; e < kTile; ++e) {
-                    x[e] = e < nvalid ? x[e] * (e < 64 ? c0 : c1) : -INFINITY;
-                    mt = fmaxf(mt, x[e]);
-                }
+                for (int e = 0; e < 64; ++e) mx0 = e < nvalid ? fmaxf(mx0, x[e]) : mx0;
+#pragma unroll
+                for (int e = 64; e < kTile; ++e) mx1 = e < nvalid ? fmaxf(mx1, x[e]) : mx1;
             }
+            const float mt = nvalid > 64 ? fmaxf(c0 * mx0, c1 * mx1) : c0 * mx0;
             const bool grow = mt > m_use + kRescaleLog2;   // always on the first tile
             float alpha = 1.0f;
             if (grow) {
-                alpha = exp2f(m_use - mt);                 // 0 on the first tile
+                alpha = ex2(m_use - mt);                   // 0 on the first tile
                 m_use = mt;
             }
+            const float nm = -m_use;
             uint32_t pk[kTile / 2];
-            float lsum = 0.0f;
+            if (nvalid == kTile) {
 #pragma unroll
-            for (int e = 0; e < kTile / 2; ++e) {
-                const __half2 hp = __floats2half2_rn(exp2f(x[2 * e] - m_use), exp2f(x[2 * e + 1] - m_use));
-                const float2 f = __half22float2(hp);
-                lsum += f.x + f.y;
-                pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
+                for (int e = 0; e < kTile / 2; ++e) {
+                    const float c = 2 * e < 64 ? c0 : c1;
+                    const __half2 hp = __floats2half2_rn(ex2(fmaf(x[2 * e], c, nm)), ex2(fmaf(x[2 * e + 1], c, nm)));
+                    pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < kTile / 2; ++e) {
+                    const float c = 2 * e < 64 ? c0 : c1;
+                    const float p0 = 2 * e < nvalid ? ex2(fmaf(x[2 * e], c, nm)) : 0.0f;
+                    const float p1 = 2 * e + 1 < nvalid ? ex2(fmaf(x[2 * e + 1], c, nm)) : 0.0f;
+                    const __half2 hp = __floats2half2_rn(p0, p1);
+                    pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
+                }
             }
-            l_run = l_run * alpha + lsum;
             // P and O are free once the previous PV product completed
             if (i >= 1) {
                 if (!(ok = wait_warp(o_done, (i - 1) & 1))) break;
                 tc::fence_after_sync();
                 if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
+                    for (int cc = 0; cc < OC; ++cc) {
                         float v[32];
                         tc::tmem_ld32(tO + lane_base + cc * 32, v);
 #pragma unroll
@@ -332,7 +379,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         if (ok && wait_warp(o_done, (ntk - 1) & 1)) {
             tc::fence_after_sync();
-            const float inv_l = 1.0f / l_run;
+            float inv_l;
+            {
+                float v[32];
+                tc::tmem_ld32(tO + lane_base + D, v);      // column D: the sum of the weights
+                inv_l = 1.0f / v[0];
+            }
             const float *vsc = a.vs + (size_t)bh * D;
             const size_t orow = (((size_t)b * n + t) * a.h + j) * D;
 #pragma unroll
