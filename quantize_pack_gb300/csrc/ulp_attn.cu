@@ -18,15 +18,21 @@
 // fp16 [B*h, D, T] (T = the live prefix rounded up to 128 rows, zero past
 // it) into a workspace, once per call, so the attention kernel moves every
 // tile with TMA straight into the tensor core's 128-byte swizzled operand
-// layout.  The attention kernel runs one CTA of six warps per (b, head,
+// layout.  The attention kernel runs one CTA of ten warps per (b, head,
 // 128-query tile):
-//   warp 4 (TMA): Q once, then K and V tiles of 128 keys, two stages each (a
+//   warp 8 (TMA): Q once, then K and V tiles of 128 keys, two stages each (a
 //     K stage frees when its S product completes, a V stage after PV);
-//   warp 5 (MMA, one thread): S_i = Q K_i^T into one of two TMEM buffers
+//   warp 9 (MMA, one thread): S_i = Q K_i^T into one of two TMEM buffers
 //     while the softmax warps work on S_{i-1}, then O += P_{i-1} V_{i-1};
-//   warps 0-3 (softmax, one query row per thread = TMEM lane): keep the
-//     running max m of the scaled logits, write P = 2^(S c - m) (fp16) to
-//     shared memory.  m moves only when the tile's max exceeds it by more
+//   warps 0-7 (softmax): query row = TMEM lane (warp % 4 picks the lane
+//     quarter), warps 0-3 take keys 0-63 of each tile and warps 4-7 keys
+//     64-127 (one K scale each); the two threads of a row exchange their
+//     maxima through shared memory.  They keep the running max m of the
+//     scaled logits and write P = 2^(S c - m) (fp16) into tensor memory over
+//     the S tile it came from; the PV product reads its A operand from
+//     there, so P needs neither shared memory nor a wait for the previous
+//     PV (the tensor pipe runs in order: QK_{i+2} overwrites that buffer
+//     only after PV_i has read it).  m moves only when the tile's max exceeds it by more
 //     than 8 (log2 units), so O is rescaled rarely; weights stay <= 2^8 and
 //     numerator and denominator share the same m, so this is exact algebra.
 //     The denominator is accumulated by the tensor core itself: each V tile
@@ -48,8 +54,9 @@ namespace ulp {
 namespace {
 
 constexpr int kTile = 128;                 // queries per CTA, keys per step
-constexpr int kSoftmaxThreads = 128;       // warps 0-3
-constexpr int kAttnThreads = 192;          // + TMA warp + MMA warp
+constexpr int kSoftmaxThreads = 256;       // warps 0-7
+constexpr int kAttnThreads = 320;          // + TMA warp 8 + MMA warp 9
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;        // S0, S1: 128 columns each; O: D + 16 (sum in column D)
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr float kRescaleLog2 = 8.0f;       // max growth (log2) absorbed without rescaling O
@@ -159,10 +166,10 @@ struct AttnLayout {
     static constexpr uint32_t q = 0;
     static constexpr uint32_t k0 = q + kBytes;
     static constexpr uint32_t v0 = k0 + 2 * kBytes;
-    static constexpr uint32_t p = v0 + 2 * vBytes;
-    static constexpr uint32_t bars = p + kTile * kTile * 2;
+    static constexpr uint32_t red = v0 + 2 * vBytes;          // softmax max exchange [2][2][128] fp32
+    static constexpr uint32_t bars = red + 4 * kTile * 4;
     // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-    // p_ready, o_done, then the TMEM address and the abort flag
+    // p_ready, o_done, o_last, then the TMEM address and the abort flag
     static constexpr uint32_t bytes = bars + 16 * 8;
 };
 
@@ -179,16 +186,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint8_t *sm = dyn_smem + ((1024u - (raw & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::bars);
     uint64_t *q_full = bars + 0, *k_full = bars + 1, *k_empty = bars + 3, *v_full = bars + 5, *v_empty = bars + 7;
-    uint64_t *s_full = bars + 9, *p_ready = bars + 11, *o_done = bars + 12;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
-    volatile int *abort = reinterpret_cast<volatile int *>(bars + 14);
+    uint64_t *s_full = bars + 9, *p_ready = bars + 11, *o_done = bars + 12, *o_last = bars + 13;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 14);
+    volatile int *abort = reinterpret_cast<volatile int *>(bars + 15);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.x * kTile, j = blockIdx.y, b = blockIdx.z;
     const int bh = b * a.h + j;
     const int n = a.n, ntk = a.ntk;
 
-    if (warp == 5) tc::tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == kMmaWarp) tc::tmem_alloc(tmem_slot, kTmemCols);
     // the constant rows of both V stages (TMA writes only the first D rows of
     // each 64-key block): row D = 1.0, rows D+1 .. D+15 = 0
     for (int x = tid; x < 4 * 16 * 8; x += kAttnThreads) {
@@ -209,6 +216,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         tc::mbar_init(p_ready, kSoftmaxThreads);
         tc::mbar_init(o_done, 1);
+        tc::mbar_init(o_last, 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -218,7 +226,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS0 = tmem, tO = tmem + 2 * kTile;
 
-    if (warp == 4) {
+    if (warp == kTmaWarp) {
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
             tc::mbar_expect_tx(q_full, Lay::kBytes);
@@ -249,11 +257,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_f16_f32(kTile, kTile), idO = tc::idesc_f16_f32(kTile, Lay::vRows);
-            const uint32_t aq = tc::smem_u32(sm + Lay::q), ap = tc::smem_u32(sm + Lay::p);
+            const uint32_t aq = tc::smem_u32(sm + Lay::q);
             bool ok = tc::mbar_wait_abortable(q_full, 0, kWaitNs, abort);
             for (int i = 0; ok && i <= ntk; ++i) {
                 if (i < ntk) {                 // S_i = Q K_i^T
@@ -274,60 +282,76 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     if (!(ok = tc::mbar_wait_abortable(v_full + s, (pi >> 1) & 1, kWaitNs, abort))) break;
                     tc::fence_after_sync();
                     const uint32_t av = tc::smem_u32(sm + Lay::v0 + s * Lay::vBytes);
+                    // A = P_{pi}: fp16 pairs in the first 64 columns of its S buffer
 #pragma unroll
                     for (int k = 0; k < kTile / 16; ++k)
-                        tc::mma_f16(tO, tc::sw128_desc_k(ap, k, kTile), tc::sw128_desc_k(av, k, Lay::vRows), idO,
-                                    (pi > 0 || k > 0) ? 1u : 0u);
+                        tc::mma_f16_ts(tO, tS0 + s * kTile + k * 8, tc::sw128_desc_k(av, k, Lay::vRows), idO,
+                                       (pi > 0 || k > 0) ? 1u : 0u);
                     tc::mma_commit(o_done);
                     tc::mma_commit(v_empty + s);
+                    if (pi == ntk - 1) tc::mma_commit(o_last);
                 }
             }
         }
-    } else {
+    } else if (warp < 8) {
         // ---------------------------------------------------------- softmax
-        const int t = t0 + tid;
+        // warp w: TMEM lane quarter w % 4 (query rows), key half g = w / 4 of
+        // every tile (one 64-key group: one K scale per thread)
+        const int g = warp >> 2, row = (warp & 3) * 32 + lane;
+        const int t = t0 + row;
         const float qa = t < n ? a.qs[(size_t)bh * a.wq + t / a.gq] * a.scale_log2 : 0.0f;
         const float *ksr = a.ks + (size_t)bh * a.wk;
-        uint8_t *prow = sm + Lay::p;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        float *red = reinterpret_cast<float *>(sm + Lay::red);   // [2 parities][2 halves][128 rows]
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         constexpr int OC = (D + 32) / 32;      // 32-column chunks of O, the sum column included
+        constexpr int OC0 = (OC + 1) / 2;      // chunks [0, OC0) rescaled by half 0, the rest by half 1
         float m_use = -INFINITY;
-        bool ok = true;
+        bool ok = true, bad = false;
         // a warp-uniform outcome, so the warp-wide TMEM accesses stay converged
         auto wait_warp = [&](uint64_t *bar, uint32_t parity) {
             return __all_sync(0xffffffffu, tc::mbar_wait_abortable(bar, parity, kWaitNs, abort)) != 0;
         };
+        // A failed wait skips the work that needs it; the softmax warps leave
+        // the loop together, at the barrier where the halves meet.
         for (int i = 0; i < ntk; ++i) {
             const int u0 = i * kTile, sb = i & 1;
-            const float c0 = qa * ksr[u0 / 64];
-            const float c1 = (u0 / 64 + 1 < a.wk) ? qa * ksr[u0 / 64 + 1] : 0.0f;
-            if (!(ok = wait_warp(s_full + sb, (i >> 1) & 1))) break;
+            const int gk = u0 / 64 + g;                    // this thread's K group
+            const float c = gk < a.wk ? qa * ksr[gk] : 0.0f;
+            const int nvalid = min(max(n - u0 - g * 64, 0), 64);
+            if (!bad) bad = !wait_warp(s_full + sb, (i >> 1) & 1);
+            float x[64];
+            float mine = -INFINITY;
+            if (!bad) {
+                tc::fence_after_sync();
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    float v[32];
+                    tc::tmem_ld32(tS0 + sb * kTile + lane_base + g * 64 + cc * 32, v);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[cc * 32 + e] = v[e];
+                }
+                // x holds integer logits; c >= 0, so the half's max scaled
+                // logit is c * (max raw logit), and each weight is 2^fma(S, c, -m)
+                float mx = -INFINITY;
+                if (nvalid == 64) {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) mx = fmaxf(mx, x[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) mx = e < nvalid ? fmaxf(mx, x[e]) : mx;
+                }
+                mine = nvalid > 0 ? c * mx : -INFINITY;
+            }
+            red[(sb * 2 + g) * kTile + row] = mine;
+            // both halves of the row have read their S columns before either
+            // writes P over the first 64 of them
+            tc::fence_before_sync();
+            if (tc::bar_or(1, kSoftmaxThreads, bad || *abort)) {
+                ok = false;
+                break;
+            }
             tc::fence_after_sync();
-            float x[kTile];
-#pragma unroll
-            for (int cc = 0; cc < kTile / 32; ++cc) {
-                float v[32];
-                tc::tmem_ld32(tS0 + sb * kTile + lane_base + cc * 32, v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[cc * 32 + e] = v[e];
-            }
-            // x holds the integer logits; the scales c0, c1 (>= 0) of the two
-            // 64-key groups are monotone, so the tile max is c * (max of the
-            // raw logits) and each weight is 2^fma(S, c, -m)
-            const int nvalid = min(kTile, n - u0);
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-            if (nvalid == kTile) {
-#pragma unroll
-                for (int e = 0; e < 64; ++e) mx0 = fmaxf(mx0, x[e]);
-#pragma unroll
-                for (int e = 64; e < kTile; ++e) mx1 = fmaxf(mx1, x[e]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 64; ++e) mx0 = e < nvalid ? fmaxf(mx0, x[e]) : mx0;
-#pragma unroll
-                for (int e = 64; e < kTile; ++e) mx1 = e < nvalid ? fmaxf(mx1, x[e]) : mx1;
-            }
-            const float mt = nvalid > 64 ? fmaxf(c0 * mx0, c1 * mx1) : c0 * mx0;
+            const float mt = fmaxf(mine, red[(sb * 2 + (g ^ 1)) * kTile + row]);
             const bool grow = mt > m_use + kRescaleLog2;   // always on the first tile
             float alpha = 1.0f;
             if (grow) {
@@ -335,49 +359,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 m_use = mt;
             }
             const float nm = -m_use;
-            uint32_t pk[kTile / 2];
-            if (nvalid == kTile) {
+            uint32_t pk[32];
+            if (nvalid == 64) {
 #pragma unroll
-                for (int e = 0; e < kTile / 2; ++e) {
-                    const float c = 2 * e < 64 ? c0 : c1;
+                for (int e = 0; e < 32; ++e) {
                     const __half2 hp = __floats2half2_rn(ex2(fmaf(x[2 * e], c, nm)), ex2(fmaf(x[2 * e + 1], c, nm)));
                     pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < kTile / 2; ++e) {
-                    const float c = 2 * e < 64 ? c0 : c1;
+                for (int e = 0; e < 32; ++e) {
                     const float p0 = 2 * e < nvalid ? ex2(fmaf(x[2 * e], c, nm)) : 0.0f;
                     const float p1 = 2 * e + 1 < nvalid ? ex2(fmaf(x[2 * e + 1], c, nm)) : 0.0f;
                     const __half2 hp = __floats2half2_rn(p0, p1);
                     pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
             }
-            // P and O are free once the previous PV product completed
-            if (i >= 1) {
-                if (!(ok = wait_warp(o_done, (i - 1) & 1))) break;
+            // P over the first 64 columns of this tile's S buffer (half g
+            // writes columns 32 g .. 32 g + 31)
+            tc::tmem_st32u(tS0 + sb * kTile + lane_base + g * 32, pk);
+            tc::tmem_st_wait();
+            // O *= alpha where the max grew: O must hold every earlier PV
+            // product first (i completions of o_done; at least i - 1 have
+            // happened, since S_i completed after PV_{i-2} in the in-order
+            // tensor pipe, so the parity wait cannot alias)
+            if (i >= 1 && __any_sync(0xffffffffu, grow)) {
+                bad = !wait_warp(o_done, (i - 1) & 1);
+                if (bad) continue;             // the next barrier takes everyone out
                 tc::fence_after_sync();
-                if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
-                    for (int cc = 0; cc < OC; ++cc) {
-                        float v[32];
-                        tc::tmem_ld32(tO + lane_base + cc * 32, v);
+                for (int cc = 0; cc < OC; ++cc) {
+                    if ((cc < OC0) != (g == 0)) continue;
+                    float v[32];
+                    tc::tmem_ld32(tO + lane_base + cc * 32, v);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] *= alpha;
-                        tc::tmem_st32(tO + lane_base + cc * 32, v);
-                    }
-                    tc::tmem_st_wait();
+                    for (int e = 0; e < 32; ++e) v[e] *= alpha;
+                    tc::tmem_st32(tO + lane_base + cc * 32, v);
                 }
+                tc::tmem_st_wait();
             }
-#pragma unroll
-            for (int c = 0; c < kTile / 8; ++c)
-                *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(tid, c, kTile)) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            tc::fence_smem_to_async();
             tc::fence_before_sync();
             tc::mbar_arrive(p_ready);
         }
-        if (ok && wait_warp(o_done, (ntk - 1) & 1)) {
+        if (ok && !bad && wait_warp(o_last, 0)) {
             tc::fence_after_sync();
             float inv_l;
             {
@@ -388,7 +412,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const float *vsc = a.vs + (size_t)bh * D;
             const size_t orow = (((size_t)b * n + t) * a.h + j) * D;
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = g * (D / 64); cc < (g + 1) * (D / 64); ++cc) {
                 float v[32];
                 tc::tmem_ld32(tO + lane_base + cc * 32, v);
                 if (t < n) {
@@ -426,10 +450,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     if (*abort) {
         if (tid == 0 && a.status) atomicExch(a.status, 1);
-        if (tid == 0) tc::mbar_wait(o_done, (ntk - 1) & 1, kWaitNs);
+        if (tid == 0) tc::mbar_wait(o_last, 0, kWaitNs);
         __syncthreads();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
