@@ -29,6 +29,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "effective HBM GB/s (amax+pack+unpack) & % of GB300 HBM peak; tokens/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def parse():
@@ -56,6 +57,17 @@ def peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense fp16 tensor TFLOP/s: the measured bf16 burst figure (fp16 runs at
+    the bf16 rate), else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured bf16 burst (cuBLAS); fp16 rate = bf16 rate"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback bf16 burst; fp16 rate = bf16 rate"
 
 
 # ------------------------------------------------------- recorded traffic
@@ -325,6 +337,31 @@ def run_ours(args, wl, rank, world, dist):
     torch.cuda.synchronize()
     kmean_ms = ks0.elapsed_time(ks1) / KM
 
+    # ---- the step after the path: attention over destination 0's outputs
+    n_att = wl.used_sequence or wl.S
+    q8, k8, v8, qsc, ksc = (o[0] for o in path.out)
+    vs0 = vs[:, :wl.h].contiguous()
+    att_ws = torch.empty(ulp.sage_attention_workspace_bytes(wl.B, wl.S, wl.h, wl.D, n_att),
+                         dtype=torch.uint8, device=dev)
+    att_out = torch.empty((wl.B, n_att, wl.h, wl.D), dtype=dt, device=dev)
+    att_status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def attend():
+        ulp.sage_attention(q8, k8, v8, qsc, ksc, vs0, n=n_att, q_group=wl.q_group,
+                           out=att_out, workspace=att_ws, status=att_status)
+
+    for _ in range(2):
+        attend()
+    ta0, ta1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    KA = 5
+    ta0.record(stream)
+    for _ in range(KA):
+        attend()
+    ta1.record(stream)
+    torch.cuda.synchronize()
+    att_ms = ta0.elapsed_time(ta1) / KA
+    att_flops = 4.0 * wl.B * wl.h * n_att * n_att * wl.D
+
     # ---- end to end through the public API with host buffers
     E = max(1, args.e2e_steps)
     pin = {n: host[n].pin_memory() for n in "qkv"}
@@ -388,6 +425,14 @@ def run_ours(args, wl, rank, world, dist):
                           "achieved_gbs": 2 * wl.N / (kmean_ms * 1e-3) / 1e9,
                           "frac": 2 * wl.N / (kmean_ms * 1e-3) / 1e9 / peak,
                           "note": "the step before the path (reads K once); not in value"},
+        "attention": {"ms": att_ms, "calls": KA, "tflops": att_flops / (att_ms * 1e-3) / 1e12,
+                      "peak": tensor_peak()[0], "peak_kind": tensor_peak()[1],
+                      "frac": att_flops / (att_ms * 1e-3) / 1e12 / tensor_peak()[0],
+                      "flops_per_call": att_flops, "status": int(att_status.item()),
+                      "note": "the step after the path: softmax attention of destination 0 "
+                              f"({wl.h} heads, {n_att} live rows, D={wl.D}) on its unpacked "
+                              "INT8/E4M3 tensors, fp16 tensor cores; 4 n^2 D flops per head; "
+                              "not in value"},
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:

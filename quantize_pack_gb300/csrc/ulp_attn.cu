@@ -323,23 +323,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             float mine = -INFINITY;
             if (!bad) {
                 tc::fence_after_sync();
+                {
+                    uint32_t r0[32], r1[32];
+                    tc::tmem_ld32_issue(tS0 + sb * kTile + lane_base + g * 64, r0);
+                    tc::tmem_ld32_issue(tS0 + sb * kTile + lane_base + g * 64 + 32, r1);
+                    tc::tmem_ld_wait(r0);
+                    tc::tmem_pin(r1);
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    float v[32];
-                    tc::tmem_ld32(tS0 + sb * kTile + lane_base + g * 64 + cc * 32, v);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) x[cc * 32 + e] = v[e];
+                    for (int e = 0; e < 32; ++e) {
+                        x[e] = __uint_as_float(r0[e]);
+                        x[32 + e] = __uint_as_float(r1[e]);
+                    }
                 }
                 // x holds integer logits; c >= 0, so the half's max scaled
-                // logit is c * (max raw logit), and each weight is 2^fma(S, c, -m)
-                float mx = -INFINITY;
+                // logit is c * (max raw logit), and each weight is 2^fma(S, c, -m).
+                // Eight independent running maxima keep the chain short.
+                float m8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
                 if (nvalid == 64) {
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) mx = fmaxf(mx, x[e]);
+                    for (int e = 0; e < 64; ++e) m8[e & 7] = fmaxf(m8[e & 7], x[e]);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) mx = e < nvalid ? fmaxf(mx, x[e]) : mx;
+                    for (int e = 0; e < 64; ++e) m8[e & 7] = e < nvalid ? fmaxf(m8[e & 7], x[e]) : m8[e & 7];
                 }
+                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
                 mine = nvalid > 0 ? c * mx : -INFINITY;
             }
             red[(sb * 2 + g) * kTile + row] = mine;
@@ -361,9 +371,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const float nm = -m_use;
             uint32_t pk[32];
             if (nvalid == 64) {
+                // exponents two at a time (packed fma.rn.f32x2: the same
+                // rounding as two fmaf)
+                const uint64_t c2 = f2pack(c, c), nm2 = f2pack(nm, nm);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const __half2 hp = __floats2half2_rn(ex2(fmaf(x[2 * e], c, nm)), ex2(fmaf(x[2 * e + 1], c, nm)));
+                    float y0, y1;
+                    f2unpack(f2fma(f2pack(x[2 * e], x[2 * e + 1]), c2, nm2), y0, y1);
+                    const __half2 hp = __floats2half2_rn(ex2(y0), ex2(y1));
                     pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
             } else {

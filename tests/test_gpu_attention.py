@@ -149,3 +149,27 @@ def test_rejects_bad_arguments():
     for kw in (dict(n=0), dict(n=129), dict(q_group=32), dict(sm_scale=-1.0)):
         with pytest.raises(ulp.UlpError):
             ulp.sage_attention(*args, **kw)
+
+
+def test_full_size_sampled_rows():
+    """The long non-aligned workload's consumer shape (one destination: B=1,
+    S = 8 x 9360, h = 5, D = 128, live prefix 74800), in the launch the bench
+    times; sampled query rows of two heads against the oracle, row by row."""
+    S, n, h, D = 8 * 9360, 74800, 5, 128
+    c = synth.attention_operands(41, B=1, S=S, h=h, D=D, n=n, q_group=128, spread=8.0)
+    got = run_gpu(c, out_dtype=torch.float32)
+    rows = [0, 1, 127, 128, 4095, 37000, 74751, 74752, n - 2, n - 1]
+    for j in (0, h - 1):
+        cj = synth.AttentionOperands(
+            np.ascontiguousarray(c.q8[:, :, j:j + 1]), np.ascontiguousarray(c.k8[:, :, j:j + 1]),
+            np.ascontiguousarray(c.v8[:, :, j:j + 1]), np.ascontiguousarray(c.q_scale[:, j:j + 1]),
+            np.ascontiguousarray(c.k_scale[:, j:j + 1]), np.ascontiguousarray(c.v_scale[:, j:j + 1]),
+            n, 128)
+        want = A.sage_attention(cj.q8, cj.k8, cj.v8, cj.q_scale, cj.k_scale, cj.v_scale, n=n,
+                                q_group=128, rows=rows)[0, :, 0]            # [rows, D]
+        Q, K, V = A.dequantize(cj.q8, cj.k8, cj.v8, cj.q_scale, cj.k_scale, cj.v_scale, n=n,
+                               q_group=128)
+        xmax = float(np.abs(Q[0, rows, 0] @ K[0, :, 0].T).max()) * D ** -0.5 / math.log(2)
+        tol = bound(n, xmax) * np.abs(V[0, :, 0]).max(axis=0)              # [D]
+        err = np.abs(got[0, rows, j] - want)
+        assert np.all(err <= tol), (j, float((err / tol).max()))
