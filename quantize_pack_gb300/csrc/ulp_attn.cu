@@ -10,9 +10,9 @@
 // 128^3 = 2^21 the integer dot products accumulate exactly in fp32; E4M3 is a
 // subset of fp16, so V widens exactly too.  The per-group scales multiply the
 // integer logits in fp32.  P = exp2(x - m) is rounded to fp16 for the PV
-// product and the softmax denominator sums the same rounded values, so the
-// output is an exact weighted mean with weights perturbed by at most 2^-11
-// relative.  Scales must be positive (they are amax / 127).
+// product, and the softmax denominator sums the unrounded values in fp32: the
+// output is a weighted mean with weights perturbed by at most 2^-11 relative,
+// times a factor within 2^-11 of 1.  Scales must be positive (amax / 127).
 //
 // Two kernels.  The widen pass writes Q and K as fp16 [B*h, T, D] and V as
 // fp16 [B*h, D, T] (T = the live prefix rounded up to 128 rows, zero past
@@ -20,10 +20,11 @@
 // tile with TMA straight into the tensor core's 128-byte swizzled operand
 // layout.  The attention kernel runs one CTA of ten warps per (b, head,
 // 128-query tile):
-//   warp 8 (TMA): Q once, then K and V tiles of 128 keys, two stages each (a
-//     K stage frees when its S product completes, a V stage after PV);
-//   warp 9 (MMA, one thread): S_i = Q K_i^T into one of two TMEM buffers
-//     while the softmax warps work on S_{i-1}, then O += P_{i-1} V_{i-1};
+//   warps 8 and 10 (TMA): Q once and K tiles of 128 keys into three stages
+//     (a stage frees when its S product completes); V tiles into two stages
+//     (freed when the PV product completes);
+//   warp 9 (MMA, one thread): S_i = Q K_i^T into one of three TMEM buffers,
+//     up to two tiles ahead of the softmax, and O += P_i V_i;
 //   warps 0-7 (softmax): query row = TMEM lane (warp % 4 picks the lane
 //     quarter), warps 0-3 take keys 0-63 of each tile and warps 4-7 keys
 //     64-127 (one K scale each); the two threads of a row exchange their
@@ -35,8 +36,8 @@
 //     only after PV_i has read it).  m moves only when the tile's max exceeds it by more
 //     than 8 (log2 units), so O is rescaled rarely; weights stay <= 2^8 and
 //     numerator and denominator share the same m, so this is exact algebra.
-//     The denominator is accumulated by the tensor core itself: each V tile
-//     carries a row of ones, so O's column D is the sum of the weights.
+//     Each thread sums its weights in fp32 (packed adds); the two halves'
+//     sums meet once at the end.
 // Every mbarrier wait is bounded: on a timeout the CTA records a status,
 // every role stops, the tensor memory is freed and nothing is written.
 #include <cuda.h>
@@ -55,9 +56,11 @@ namespace {
 
 constexpr int kTile = 128;                 // queries per CTA, keys per step
 constexpr int kSoftmaxThreads = 256;       // warps 0-7
-constexpr int kAttnThreads = 320;          // + TMA warp 8 + MMA warp 9
-constexpr int kTmaWarp = 8, kMmaWarp = 9;
-constexpr uint32_t kTmemCols = 512;        // S0, S1: 128 columns each; O: D + 16 (sum in column D)
+constexpr int kAttnThreads = 352;          // + K/Q TMA warp 8, MMA warp 9, V TMA warp 10
+constexpr int kKTmaWarp = 8, kMmaWarp = 9, kVTmaWarp = 10;
+constexpr int kSBufs = 3;                  // S / P buffers in TMEM
+constexpr int kKStages = 3, kVStages = 2;  // shared-memory stages
+constexpr uint32_t kTmemCols = 512;        // S0, S1, S2: 128 columns each; O: D columns
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr float kRescaleLog2 = 8.0f;       // max growth (log2) absorbed without rescaling O
 
@@ -155,23 +158,36 @@ struct AttnArgs {
     float scale_log2;                      // sm_scale * log2(e)
 };
 
-// A V tile holds D channel rows and 16 more: a row of ones (so the PV product
-// also accumulates the softmax denominator, in O's column D) and 15 zero rows.
 template <int D>
 struct AttnLayout {
-    static constexpr int vRows = D + 16;
     static constexpr uint32_t kBytes = kTile * D * 2;         // one Q or K tile
-    static constexpr uint32_t vBytes = vRows * kTile * 2;     // one V tile
-    static constexpr uint32_t vLoadBytes = D * kTile * 2;     // what TMA writes of it
+    static constexpr uint32_t vBytes = D * kTile * 2;         // one V tile
     static constexpr uint32_t q = 0;
-    static constexpr uint32_t k0 = q + kBytes;
-    static constexpr uint32_t v0 = k0 + 2 * kBytes;
-    static constexpr uint32_t red = v0 + 2 * vBytes;          // softmax max exchange [2][2][128] fp32
-    static constexpr uint32_t bars = red + 4 * kTile * 4;
-    // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-    // p_ready, o_done, o_last, then the TMEM address and the abort flag
-    static constexpr uint32_t bytes = bars + 16 * 8;
+    static constexpr uint32_t k0 = q + kBytes;                // kKStages K tiles
+    static constexpr uint32_t v0 = k0 + kKStages * kBytes;    // kVStages V tiles
+    // softmax exchange, fp32 [3][2][128]: the row maxima of even and odd
+    // tiles, then the row sums; [.][g][row] is written by half g
+    static constexpr uint32_t red = v0 + kVStages * vBytes;
+    static constexpr uint32_t bars = red + 6 * kTile * 4;
+    static constexpr uint32_t bytes = bars + 32 * 8;
 };
+
+// Barrier slots (uint64 each) after Lay::bars.
+enum : int {
+    kQFull = 0,
+    kKFull = 1,                                        // [kKStages]
+    kKEmpty = kKFull + kKStages,                       // [kKStages]
+    kVFull = kKEmpty + kKStages,                       // [kVStages]
+    kVEmpty = kVFull + kVStages,                       // [kVStages]
+    kSFull = kVEmpty + kVStages,                       // [kSBufs]
+    kPReady = kSFull + kSBufs,                         // [kSBufs]
+    kODone = kPReady + kSBufs,                         // [2], by PV parity
+    kOLast = kODone + 2,
+    kTmemSlot = kOLast + 1,
+    kAbortSlot = kTmemSlot + 1,
+    kNumSlots = kAbortSlot + 1
+};
+static_assert(kNumSlots <= 32, "barrier area");
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -185,10 +201,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t raw = tc::smem_u32(dyn_smem);
     uint8_t *sm = dyn_smem + ((1024u - (raw & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::bars);
-    uint64_t *q_full = bars + 0, *k_full = bars + 1, *k_empty = bars + 3, *v_full = bars + 5, *v_empty = bars + 7;
-    uint64_t *s_full = bars + 9, *p_ready = bars + 11, *o_done = bars + 12, *o_last = bars + 13;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 14);
-    volatile int *abort = reinterpret_cast<volatile int *>(bars + 15);
+    uint64_t *q_full = bars + kQFull, *k_full = bars + kKFull, *k_empty = bars + kKEmpty;
+    uint64_t *v_full = bars + kVFull, *v_empty = bars + kVEmpty, *s_full = bars + kSFull;
+    uint64_t *p_ready = bars + kPReady, *o_done = bars + kODone, *o_last = bars + kOLast;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kTmemSlot);
+    volatile int *abort = reinterpret_cast<volatile int *>(bars + kAbortSlot);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.x * kTile, j = blockIdx.y, b = blockIdx.z;
@@ -196,26 +213,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int n = a.n, ntk = a.ntk;
 
     if (warp == kMmaWarp) tc::tmem_alloc(tmem_slot, kTmemCols);
-    // the constant rows of both V stages (TMA writes only the first D rows of
-    // each 64-key block): row D = 1.0, rows D+1 .. D+15 = 0
-    for (int x = tid; x < 4 * 16 * 8; x += kAttnThreads) {
-        const int blk = x / 128, r = (x / 8) % 16, c = x % 8;
-        uint8_t *row = sm + Lay::v0 + (blk >> 1) * Lay::vBytes + (blk & 1) * (Lay::vRows * 128) + (D + r) * 128;
-        const uint32_t one2 = 0x3C003C00u;   // two fp16 ones
-        reinterpret_cast<uint4 *>(row)[c] = r == 0 ? make_uint4(one2, one2, one2, one2) : make_uint4(0, 0, 0, 0);
-    }
-    tc::fence_smem_to_async();
     if (tid == 0) {
         tc::mbar_init(q_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             tc::mbar_init(k_full + s, 1);
             tc::mbar_init(k_empty + s, 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
             tc::mbar_init(v_full + s, 1);
             tc::mbar_init(v_empty + s, 1);
-            tc::mbar_init(s_full + s, 1);
         }
-        tc::mbar_init(p_ready, kSoftmaxThreads);
+        for (int s = 0; s < kSBufs; ++s) {
+            tc::mbar_init(s_full + s, 1);
+            tc::mbar_init(p_ready + s, kSoftmaxThreads);
+        }
         tc::mbar_init(o_done, 1);
+        tc::mbar_init(o_done + 1, 1);
         tc::mbar_init(o_last, 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -224,73 +237,94 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS0 = tmem, tO = tmem + 2 * kTile;
+    const uint32_t tS0 = tmem, tO = tmem + kSBufs * kTile;
 
-    if (warp == kTmaWarp) {
-        // ------------------------------------------------------- TMA producer
+    if (warp == kKTmaWarp) {
+        // --------------------------------------------------- TMA: Q, then K
         if (lane == 0) {
             tc::mbar_expect_tx(q_full, Lay::kBytes);
             for (int kb = 0; kb < D / 64; ++kb)
                 tc::tma_load_3d(sm + Lay::q + kb * (kTile * 128), &tm_q, kb * 64, t0, bh, q_full);
-            // K stages free up when S = Q K^T completes, V stages when PV
-            // does, so K runs ahead of V
-            int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};   // last tile loaded into each stage
+            int last[kKStages];
+            for (int s = 0; s < kKStages; ++s) last[s] = -1;
             for (int i = 0; i < ntk; ++i) {
-                const int s = i & 1;
-                if (i >= 2 && !tc::mbar_wait_abortable(k_empty + s, ((i >> 1) - 1) & 1, kWaitNs, abort)) break;
+                const int s = i % kKStages;
+                // a K stage frees when its S product completes
+                if (i >= kKStages &&
+                    !tc::mbar_wait_abortable(k_empty + s, ((i / kKStages) - 1) & 1, kWaitNs, abort))
+                    break;
                 tc::mbar_expect_tx(k_full + s, Lay::kBytes);
-                uint8_t *kd = sm + Lay::k0 + s * Lay::kBytes, *vd = sm + Lay::v0 + s * Lay::vBytes;
+                uint8_t *kd = sm + Lay::k0 + s * Lay::kBytes;
                 for (int kb = 0; kb < D / 64; ++kb)
                     tc::tma_load_3d(kd + kb * (kTile * 128), &tm_k, kb * 64, i * kTile, bh, k_full + s);
-                last_k[s] = i;
-                if (i >= 2 && !tc::mbar_wait_abortable(v_empty + s, ((i >> 1) - 1) & 1, kWaitNs, abort)) break;
-                tc::mbar_expect_tx(v_full + s, Lay::vLoadBytes);
-                for (int c = 0; c < 2; ++c)
-                    tc::tma_load_3d(vd + c * (Lay::vRows * 128), &tm_v, i * kTile + c * 64, 0, bh, v_full + s);
-                last_v[s] = i;
+                last[s] = i;
             }
             if (*abort) {                      // let the copies in flight land
                 tc::mbar_wait(q_full, 0, kWaitNs);
-                for (int s = 0; s < 2; ++s) {
-                    if (last_k[s] >= 0) tc::mbar_wait(k_full + s, (last_k[s] >> 1) & 1, kWaitNs);
-                    if (last_v[s] >= 0) tc::mbar_wait(v_full + s, (last_v[s] >> 1) & 1, kWaitNs);
-                }
+                for (int s = 0; s < kKStages; ++s)
+                    if (last[s] >= 0) tc::mbar_wait(k_full + s, (last[s] / kKStages) & 1, kWaitNs);
+            }
+        }
+    } else if (warp == kVTmaWarp) {
+        // --------------------------------------------------------- TMA: V
+        if (lane == 0) {
+            int last[kVStages];
+            for (int s = 0; s < kVStages; ++s) last[s] = -1;
+            for (int i = 0; i < ntk; ++i) {
+                const int s = i % kVStages;
+                // a V stage frees when its PV product completes
+                if (i >= kVStages &&
+                    !tc::mbar_wait_abortable(v_empty + s, ((i / kVStages) - 1) & 1, kWaitNs, abort))
+                    break;
+                tc::mbar_expect_tx(v_full + s, Lay::vBytes);
+                uint8_t *vd = sm + Lay::v0 + s * Lay::vBytes;
+                for (int c = 0; c < 2; ++c)
+                    tc::tma_load_3d(vd + c * (D * 128), &tm_v, i * kTile + c * 64, 0, bh, v_full + s);
+                last[s] = i;
+            }
+            if (*abort) {
+                for (int s = 0; s < kVStages; ++s)
+                    if (last[s] >= 0) tc::mbar_wait(v_full + s, (last[s] / kVStages) & 1, kWaitNs);
             }
         }
     } else if (warp == kMmaWarp) {
         // -------------------------------------------------------- MMA issuer
+        // S_i = Q K_i^T runs up to two tiles ahead of the softmax (three S
+        // buffers); S_{i+3} is issued after PV_i, which read P_i from that
+        // buffer (the tensor pipe runs in order).
         if (lane == 0) {
-            constexpr uint32_t idS = tc::idesc_f16_f32(kTile, kTile), idO = tc::idesc_f16_f32(kTile, Lay::vRows);
+            constexpr uint32_t idS = tc::idesc_f16_f32(kTile, kTile), idO = tc::idesc_f16_f32(kTile, D);
             const uint32_t aq = tc::smem_u32(sm + Lay::q);
             bool ok = tc::mbar_wait_abortable(q_full, 0, kWaitNs, abort);
-            for (int i = 0; ok && i <= ntk; ++i) {
-                if (i < ntk) {                 // S_i = Q K_i^T
-                    const int s = i & 1;
-                    if (!(ok = tc::mbar_wait_abortable(k_full + s, (i >> 1) & 1, kWaitNs, abort))) break;
+            int nq = 0;                        // next S product to issue
+            for (int pv = 0; ok && pv < ntk; ++pv) {
+                for (; nq < ntk && nq <= pv + kSBufs - 1; ++nq) {
+                    const int ks = nq % kKStages, sb = nq % kSBufs;
+                    if (!(ok = tc::mbar_wait_abortable(k_full + ks, (nq / kKStages) & 1, kWaitNs, abort))) break;
                     tc::fence_after_sync();
-                    const uint32_t ak = tc::smem_u32(sm + Lay::k0 + s * Lay::kBytes);
+                    const uint32_t ak = tc::smem_u32(sm + Lay::k0 + ks * Lay::kBytes);
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k)
-                        tc::mma_f16(tS0 + s * kTile, tc::sw128_desc_k(aq, k, kTile), tc::sw128_desc_k(ak, k, kTile),
-                                    idS, k > 0);
-                    tc::mma_commit(s_full + s);
-                    tc::mma_commit(k_empty + s);
+                        tc::mma_f16(tS0 + sb * kTile, tc::sw128_desc_k(aq, k, kTile),
+                                    tc::sw128_desc_k(ak, k, kTile), idS, k > 0);
+                    tc::mma_commit(s_full + sb);
+                    tc::mma_commit(k_empty + ks);
                 }
-                if (i >= 1) {                  // O += P_{i-1} V_{i-1}
-                    const int pi = i - 1, s = pi & 1;
-                    if (!(ok = tc::mbar_wait_abortable(p_ready, pi & 1, kWaitNs, abort))) break;
-                    if (!(ok = tc::mbar_wait_abortable(v_full + s, (pi >> 1) & 1, kWaitNs, abort))) break;
-                    tc::fence_after_sync();
-                    const uint32_t av = tc::smem_u32(sm + Lay::v0 + s * Lay::vBytes);
-                    // A = P_{pi}: fp16 pairs in the first 64 columns of its S buffer
+                if (!ok) break;
+                // O += P_pv V_pv, A = P_pv: fp16 pairs in the first 64
+                // columns of its S buffer
+                const int sb = pv % kSBufs, vs = pv % kVStages;
+                if (!(ok = tc::mbar_wait_abortable(p_ready + sb, (pv / kSBufs) & 1, kWaitNs, abort))) break;
+                if (!(ok = tc::mbar_wait_abortable(v_full + vs, (pv / kVStages) & 1, kWaitNs, abort))) break;
+                tc::fence_after_sync();
+                const uint32_t av = tc::smem_u32(sm + Lay::v0 + vs * Lay::vBytes);
 #pragma unroll
-                    for (int k = 0; k < kTile / 16; ++k)
-                        tc::mma_f16_ts(tO, tS0 + s * kTile + k * 8, tc::sw128_desc_k(av, k, Lay::vRows), idO,
-                                       (pi > 0 || k > 0) ? 1u : 0u);
-                    tc::mma_commit(o_done);
-                    tc::mma_commit(v_empty + s);
-                    if (pi == ntk - 1) tc::mma_commit(o_last);
-                }
+                for (int k = 0; k < kTile / 16; ++k)
+                    tc::mma_f16_ts(tO, tS0 + sb * kTile + k * 8, tc::sw128_desc_k(av, k, D), idO,
+                                   (pv > 0 || k > 0) ? 1u : 0u);
+                tc::mma_commit(o_done + (pv & 1));
+                tc::mma_commit(v_empty + vs);
+                if (pv == ntk - 1) tc::mma_commit(o_last);
             }
         }
     } else if (warp < 8) {
@@ -301,11 +335,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int t = t0 + row;
         const float qa = t < n ? a.qs[(size_t)bh * a.wq + t / a.gq] * a.scale_log2 : 0.0f;
         const float *ksr = a.ks + (size_t)bh * a.wk;
-        float *red = reinterpret_cast<float *>(sm + Lay::red);   // [2 parities][2 halves][128 rows]
+        float *red = reinterpret_cast<float *>(sm + Lay::red);   // [3][2 halves][128 rows]
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        constexpr int OC = (D + 32) / 32;      // 32-column chunks of O, the sum column included
+        constexpr int OC = D / 32;             // 32-column chunks of O
         constexpr int OC0 = (OC + 1) / 2;      // chunks [0, OC0) rescaled by half 0, the rest by half 1
         float m_use = -INFINITY;
+        uint64_t l2 = f2pack(0.0f, 0.0f);     // this half's weight sum, in two lanes
         bool ok = true, bad = false;
         // a warp-uniform outcome, so the warp-wide TMEM accesses stay converged
         auto wait_warp = [&](uint64_t *bar, uint32_t parity) {
@@ -314,11 +349,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // A failed wait skips the work that needs it; the softmax warps leave
         // the loop together, at the barrier where the halves meet.
         for (int i = 0; i < ntk; ++i) {
-            const int u0 = i * kTile, sb = i & 1;
+            const int u0 = i * kTile, sb = i % kSBufs;
             const int gk = u0 / 64 + g;                    // this thread's K group
             const float c = gk < a.wk ? qa * ksr[gk] : 0.0f;
             const int nvalid = min(max(n - u0 - g * 64, 0), 64);
-            if (!bad) bad = !wait_warp(s_full + sb, (i >> 1) & 1);
+            if (!bad) bad = !wait_warp(s_full + sb, (i / kSBufs) & 1);
             float x[64];
             float mine = -INFINITY;
             if (!bad) {
@@ -352,7 +387,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                        fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
                 mine = nvalid > 0 ? c * mx : -INFINITY;
             }
-            red[(sb * 2 + g) * kTile + row] = mine;
+            red[((i & 1) * 2 + g) * kTile + row] = mine;
             // both halves of the row have read their S columns before either
             // writes P over the first 64 of them
             tc::fence_before_sync();
@@ -361,12 +396,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 break;
             }
             tc::fence_after_sync();
-            const float mt = fmaxf(mine, red[(sb * 2 + (g ^ 1)) * kTile + row]);
+            const float mt = fmaxf(mine, red[((i & 1) * 2 + (g ^ 1)) * kTile + row]);
             const bool grow = mt > m_use + kRescaleLog2;   // always on the first tile
             float alpha = 1.0f;
             if (grow) {
                 alpha = ex2(m_use - mt);                   // 0 on the first tile
                 m_use = mt;
+                l2 = f2mul(l2, f2pack(alpha, alpha));
             }
             const float nm = -m_use;
             uint32_t pk[32];
@@ -378,7 +414,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int e = 0; e < 32; ++e) {
                     float y0, y1;
                     f2unpack(f2fma(f2pack(x[2 * e], x[2 * e + 1]), c2, nm2), y0, y1);
-                    const __half2 hp = __floats2half2_rn(ex2(y0), ex2(y1));
+                    const float p0 = ex2(y0), p1 = ex2(y1);
+                    l2 = f2add(l2, f2pack(p0, p1));
+                    const __half2 hp = __floats2half2_rn(p0, p1);
                     pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
             } else {
@@ -386,6 +424,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int e = 0; e < 32; ++e) {
                     const float p0 = 2 * e < nvalid ? ex2(fmaf(x[2 * e], c, nm)) : 0.0f;
                     const float p1 = 2 * e + 1 < nvalid ? ex2(fmaf(x[2 * e + 1], c, nm)) : 0.0f;
+                    l2 = f2add(l2, f2pack(p0, p1));
                     const __half2 hp = __floats2half2_rn(p0, p1);
                     pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
@@ -394,12 +433,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // writes columns 32 g .. 32 g + 31)
             tc::tmem_st32u(tS0 + sb * kTile + lane_base + g * 32, pk);
             tc::tmem_st_wait();
-            // O *= alpha where the max grew: O must hold every earlier PV
-            // product first (i completions of o_done; at least i - 1 have
-            // happened, since S_i completed after PV_{i-2} in the in-order
-            // tensor pipe, so the parity wait cannot alias)
+            // O *= alpha where the max grew: O must first hold PV_{i-1}.
+            // PV products alternate between two barriers; S_i completed after
+            // PV_{i-3}, so barrier (i-1) & 1 has completed either the phase
+            // waited for or the one before it, and the parity cannot alias.
             if (i >= 1 && __any_sync(0xffffffffu, grow)) {
-                bad = !wait_warp(o_done, (i - 1) & 1);
+                bad = !wait_warp(o_done + ((i - 1) & 1), ((i - 1) >> 1) & 1);
                 if (bad) continue;             // the next barrier takes everyone out
                 tc::fence_after_sync();
 #pragma unroll
@@ -414,16 +453,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 tc::tmem_st_wait();
             }
             tc::fence_before_sync();
-            tc::mbar_arrive(p_ready);
+            tc::mbar_arrive(p_ready + sb);
         }
-        if (ok && !bad && wait_warp(o_last, 0)) {
+        // the two halves' sums meet (every softmax thread reaches this point)
+        float l0, l1;
+        f2unpack(l2, l0, l1);
+        red[(4 + g) * kTile + row] = l0 + l1;
+        const bool fine = !tc::bar_or(1, kSoftmaxThreads, !ok || bad || *abort);
+        const float inv_l = 1.0f / (red[4 * kTile + row] + red[5 * kTile + row]);
+        if (fine && wait_warp(o_last, 0)) {
             tc::fence_after_sync();
-            float inv_l;
-            {
-                float v[32];
-                tc::tmem_ld32(tO + lane_base + D, v);      // column D: the sum of the weights
-                inv_l = 1.0f / v[0];
-            }
             const float *vsc = a.vs + (size_t)bh * D;
             const size_t orow = (((size_t)b * n + t) * a.h + j) * D;
 #pragma unroll

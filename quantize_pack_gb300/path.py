@@ -66,10 +66,11 @@ class UlyssesLowpPath:
         return 0 if self.fold_exchange else P_copies(self.P)
 
     def run(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, k_mean: torch.Tensor,
-            v_scale: torch.Tensor, on_pack=None):
+            v_scale: torch.Tensor, on_pack=None, out=None):
         """q, k, v: stacked shards [P, B, L, H, D]; k_mean [B, H, D] (input
         dtype); v_scale [B, H, D] fp32.  Returns the per-destination outputs
-        (q8, k8, v8, q_scale, k_scale), each with a leading P axis.
+        (q8, k8, v8, q_scale, k_scale), each with a leading P axis, in
+        ``out`` (a tuple from ``new_outputs()``) or ``self.out``.
         ``on_pack`` (optional) is a pair of callables run right before and
         after the pack launch (used to time it)."""
         P, L = self.P, self.L
@@ -97,7 +98,68 @@ class UlyssesLowpPath:
         return ulp.unpack_for_sage(self.recv, batch_size=self.B, local_sequence=L,
                                    local_heads=self.h, head_dim=self.D, world_size=P,
                                    aligned=self.aligned, scale_sequence=self.scale_sequence,
-                                   q_group=self.q_group, out=self.out, enable_pdl=self.pdl)
+                                   q_group=self.q_group, out=self.out if out is None else out,
+                                   enable_pdl=self.pdl)
+
+    def new_outputs(self):
+        """A fresh set of device output tensors shaped like ``self.out``."""
+        return tuple(torch.empty_like(o) for o in self.out)
+
+    def new_inputs(self):
+        """Device input tensors (q, k, v, k_mean, v_scale) for one step."""
+        P, B, L, H, D = self.P, self.B, self.L, self.H, self.D
+        dev = self.device
+        x = dict(dtype=self.dtype, device=dev)
+        return (torch.empty((P, B, L, H, D), **x), torch.empty((P, B, L, H, D), **x),
+                torch.empty((P, B, L, H, D), **x), torch.empty((B, H, D), **x),
+                torch.empty((B, H, D), dtype=torch.float32, device=dev))
+
+    def run_host(self, host_inputs, host_outputs, pipe=None):
+        """Run consecutive steps from pinned host memory to pinned host memory.
+
+        host_inputs[i] = (q, k, v, k_mean, v_scale) and host_outputs[i] = the
+        five outputs, all pinned CPU tensors shaped like ``new_inputs()`` /
+        ``self.out``.  Step i's upload, its kernels and its download run on
+        three streams with two device buffer sets, so step i + 1's upload
+        overlaps step i's kernels and download (the two copy directions run
+        concurrently).  Returns once every download has been issued; the
+        caller synchronises (``torch.cuda.synchronize``) before reading.
+        ``pipe`` (from ``host_pipe()``) holds the device buffers and streams;
+        a new one is made when None."""
+        pipe = self.host_pipe() if pipe is None else pipe
+        compute = torch.cuda.current_stream(self.device)
+        for i, (hin, hout) in enumerate(zip(host_inputs, host_outputs)):
+            s = i % 2
+            din, dout = pipe["inputs"][s], pipe["outputs"][s]
+            up = pipe["up"]
+            up.wait_event(pipe["in_free"][s])            # step i-2's kernels are done with din
+            with torch.cuda.stream(up):
+                for d, h in zip(din, hin):
+                    d.copy_(h, non_blocking=True)
+                pipe["in_ready"][s].record(up)
+            compute.wait_event(pipe["in_ready"][s])
+            compute.wait_event(pipe["out_free"][s])      # step i-2's download is done with dout
+            self.run(*din, out=dout)
+            pipe["in_free"][s].record(compute)
+            pipe["out_ready"][s].record(compute)
+            down = pipe["down"]
+            down.wait_event(pipe["out_ready"][s])
+            with torch.cuda.stream(down):
+                for h, d in zip(hout, dout):
+                    h.copy_(d, non_blocking=True)
+                pipe["out_free"][s].record(down)
+        compute.wait_stream(pipe["down"])
+
+    def host_pipe(self):
+        """Device buffers, streams and events of ``run_host``."""
+        ev = lambda: [torch.cuda.Event(), torch.cuda.Event()]
+        pipe = {"inputs": [self.new_inputs(), self.new_inputs()],
+                "outputs": [self.new_outputs(), self.new_outputs()],
+                "up": torch.cuda.Stream(self.device), "down": torch.cuda.Stream(self.device),
+                "in_ready": ev(), "in_free": ev(), "out_ready": ev(), "out_free": ev()}
+        for e in pipe["in_free"] + pipe["out_free"]:      # nothing to wait for yet
+            e.record(torch.cuda.current_stream(self.device))
+        return pipe
 
     def capture(self, q, k, v, k_mean, v_scale):
         """Record one step on these input tensors as a CUDA graph; replay it

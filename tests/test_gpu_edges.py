@@ -148,3 +148,27 @@ def test_cuda_graph_replay_with_new_inputs():
         torch.cuda.synchronize()
         for i, name in enumerate(["q8", "k8", "v8", "q_scale", "k_scale"]):
             gh.assert_bits_equal(path.out[i], np.stack([res["out"][p][i] for p in range(wl.P)]), name)
+
+
+def test_host_pipeline_runs_consecutive_steps():
+    """UlyssesLowpPath.run_host: three steps with different inputs, pinned
+    host memory in and out, uploads overlapping the previous step's kernels
+    and downloads; every step's outputs equal the oracle's."""
+    wl = hp.PADDING_R
+    path = UlyssesLowpPath(B=wl.B, L=wl.L, H=wl.H, D=wl.D, world_size=wl.P,
+                           dtype=gh.torch_dtype(wl.dtype), used_sequence=wl.used_sequence,
+                           scale_sequence=wl.scale_sequence)
+    host_in, want = [], []
+    for seed in (51, 52, 53):
+        inp = synth.make_inputs(wl.replace(seed=seed, name=f"{wl.name}_h{seed}"))
+        res = hp.run_oracle(inp)
+        dev = gh.to_device(inp, device="cpu")
+        host_in.append(tuple(t.pin_memory() for t in dev))
+        want.append([np.stack([res["out"][p][i] for p in range(wl.P)]) for i in range(5)])
+    host_out = [tuple(torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in path.out)
+                for _ in host_in]
+    path.run_host(host_in, host_out)
+    torch.cuda.synchronize()
+    for step, (got, exp) in enumerate(zip(host_out, want)):
+        for i, name in enumerate(["q8", "k8", "v8", "q_scale", "k_scale"]):
+            gh.assert_bits_equal(got[i], exp[i], f"step {step} {name}")
