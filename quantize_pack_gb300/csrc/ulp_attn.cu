@@ -10,9 +10,9 @@
 // 128^3 = 2^21 the integer dot products accumulate exactly in fp32; E4M3 is a
 // subset of fp16, so V widens exactly too.  The per-group scales multiply the
 // integer logits in fp32.  P = exp2(x - m) is rounded to fp16 for the PV
-// product, and the softmax denominator sums the unrounded values in fp32: the
-// output is a weighted mean with weights perturbed by at most 2^-11 relative,
-// times a factor within 2^-11 of 1.  Scales must be positive (amax / 127).
+// product and the softmax denominator sums the same rounded values, so the
+// output is an exact weighted mean with weights perturbed by at most 2^-11
+// relative.  Scales must be positive (they are amax / 127).
 //
 // Two kernels.  The widen pass writes Q and K as fp16 [B*h, T, D] and V as
 // fp16 [B*h, D, T] (T = the live prefix rounded up to 128 rows, zero past
@@ -20,11 +20,13 @@
 // tile with TMA straight into the tensor core's 128-byte swizzled operand
 // layout.  The attention kernel runs one CTA of ten warps per (b, head,
 // 128-query tile):
-//   warps 8 and 10 (TMA): Q once and K tiles of 128 keys into three stages
-//     (a stage frees when its S product completes); V tiles into two stages
-//     (freed when the PV product completes);
-//   warp 9 (MMA, one thread): S_i = Q K_i^T into one of three TMEM buffers,
-//     up to two tiles ahead of the softmax, and O += P_i V_i;
+//   warps 8 and 10 (TMA): K tiles of 128 keys into three stages (a stage
+//     frees when its S product completes), V tiles into two stages (freed
+//     when the PV product completes);
+//   warp 9 (MMA, one thread): S_i = Q K_i^T into one of two TMEM buffers, a
+//     tile ahead of the softmax, and O += P_i V_i; Q and P are the A
+//     operands in tensor memory, so the products read only K and V from
+//     shared memory;
 //   warps 0-7 (softmax): query row = TMEM lane (warp % 4 picks the lane
 //     quarter), warps 0-3 take keys 0-63 of each tile and warps 4-7 keys
 //     64-127 (one K scale each); the two threads of a row exchange their
@@ -36,8 +38,8 @@
 //     only after PV_i has read it).  m moves only when the tile's max exceeds it by more
 //     than 8 (log2 units), so O is rescaled rarely; weights stay <= 2^8 and
 //     numerator and denominator share the same m, so this is exact algebra.
-//     Each thread sums its weights in fp32 (packed adds); the two halves'
-//     sums meet once at the end.
+//     The denominator is accumulated by the tensor core itself: each V tile
+//     carries a row of ones, so O's column D is the sum of the weights.
 // Every mbarrier wait is bounded: on a timeout the CTA records a status,
 // every role stops, the tensor memory is freed and nothing is written.
 #include <cuda.h>
@@ -58,9 +60,9 @@ constexpr int kTile = 128;                 // queries per CTA, keys per step
 constexpr int kSoftmaxThreads = 256;       // warps 0-7
 constexpr int kAttnThreads = 352;          // + K/Q TMA warp 8, MMA warp 9, V TMA warp 10
 constexpr int kKTmaWarp = 8, kMmaWarp = 9, kVTmaWarp = 10;
-constexpr int kSBufs = 3;                  // S / P buffers in TMEM
+constexpr int kSBufs = 2;                  // S / P buffers in TMEM
 constexpr int kKStages = 3, kVStages = 2;  // shared-memory stages
-constexpr uint32_t kTmemCols = 512;        // S0, S1, S2: 128 columns each; O: D columns
+constexpr uint32_t kTmemCols = 512;        // S0, S1: 128 columns each; O: D + 16 (sum in column D); Q: D / 2
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr float kRescaleLog2 = 8.0f;       // max growth (log2) absorbed without rescaling O
 
@@ -150,25 +152,29 @@ __global__ void __launch_bounds__(256) attn_widen_kernel(WidenArgs a)
 // ------------------------------------------------------- attention kernel
 
 struct AttnArgs {
+    const uint16_t *q16;                   // widened Q [B*h, T, D]
     const float *qs, *ks, *vs;
     void *out;
     int *status;
     int out_dtype;
-    int h, n, gq, wq, wk, ntk;
+    int h, n, gq, wq, wk, ntk, T;
     float scale_log2;                      // sm_scale * log2(e)
 };
 
+// A V tile holds D channel rows and 16 more: a row of ones (so the PV product
+// also accumulates the softmax denominator, in O's column D) and 15 zero rows.
 template <int D>
 struct AttnLayout {
-    static constexpr uint32_t kBytes = kTile * D * 2;         // one Q or K tile
-    static constexpr uint32_t vBytes = D * kTile * 2;         // one V tile
-    static constexpr uint32_t q = 0;
-    static constexpr uint32_t k0 = q + kBytes;                // kKStages K tiles
+    static constexpr int vRows = D + 16;
+    static constexpr uint32_t kBytes = kTile * D * 2;         // one K tile
+    static constexpr uint32_t vBytes = vRows * kTile * 2;     // one V tile
+    static constexpr uint32_t vLoadBytes = D * kTile * 2;     // what TMA writes of it
+    static constexpr uint32_t k0 = 0;                         // kKStages K tiles
     static constexpr uint32_t v0 = k0 + kKStages * kBytes;    // kVStages V tiles
-    // softmax exchange, fp32 [3][2][128]: the row maxima of even and odd
-    // tiles, then the row sums; [.][g][row] is written by half g
+    // softmax max exchange, fp32 [2][2][128]: even and odd tiles; [.][g][row]
+    // is written by half g
     static constexpr uint32_t red = v0 + kVStages * vBytes;
-    static constexpr uint32_t bars = red + 6 * kTile * 4;
+    static constexpr uint32_t bars = red + 4 * kTile * 4;
     static constexpr uint32_t bytes = bars + 32 * 8;
 };
 
@@ -191,8 +197,8 @@ static_assert(kNumSlots <= 32, "barrier area");
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    sage_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v, AttnArgs a)
+    sage_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                          AttnArgs a)
 {
     using Lay = AttnLayout<D>;
     extern __shared__ uint8_t dyn_smem[];
@@ -213,8 +219,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int n = a.n, ntk = a.ntk;
 
     if (warp == kMmaWarp) tc::tmem_alloc(tmem_slot, kTmemCols);
+    // the constant rows of every V stage (TMA writes only the first D rows of
+    // each 64-key block): row D = 1.0, rows D+1 .. D+15 = 0
+    for (int x = tid; x < kVStages * 2 * 16 * 8; x += kAttnThreads) {
+        const int blk = x / 128, r = (x / 8) % 16, c = x % 8;
+        uint8_t *row = sm + Lay::v0 + (blk >> 1) * Lay::vBytes + (blk & 1) * (Lay::vRows * 128) + (D + r) * 128;
+        const uint32_t one2 = 0x3C003C00u;   // two fp16 ones
+        reinterpret_cast<uint4 *>(row)[c] = r == 0 ? make_uint4(one2, one2, one2, one2) : make_uint4(0, 0, 0, 0);
+    }
+    tc::fence_smem_to_async();
     if (tid == 0) {
-        tc::mbar_init(q_full, 1);
+        tc::mbar_init(q_full, kSoftmaxThreads / 2);      // the half-0 softmax threads write Q
         for (int s = 0; s < kKStages; ++s) {
             tc::mbar_init(k_full + s, 1);
             tc::mbar_init(k_empty + s, 1);
@@ -237,14 +252,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS0 = tmem, tO = tmem + kSBufs * kTile;
+    // O takes D + 16 columns, read in 32-column chunks: Q starts after them
+    const uint32_t tS0 = tmem, tO = tmem + kSBufs * kTile, tQ = tO + (D + 32);
 
     if (warp == kKTmaWarp) {
-        // --------------------------------------------------- TMA: Q, then K
+        // --------------------------------------------------------- TMA: K
         if (lane == 0) {
-            tc::mbar_expect_tx(q_full, Lay::kBytes);
-            for (int kb = 0; kb < D / 64; ++kb)
-                tc::tma_load_3d(sm + Lay::q + kb * (kTile * 128), &tm_q, kb * 64, t0, bh, q_full);
             int last[kKStages];
             for (int s = 0; s < kKStages; ++s) last[s] = -1;
             for (int i = 0; i < ntk; ++i) {
@@ -260,7 +273,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 last[s] = i;
             }
             if (*abort) {                      // let the copies in flight land
-                tc::mbar_wait(q_full, 0, kWaitNs);
                 for (int s = 0; s < kKStages; ++s)
                     if (last[s] >= 0) tc::mbar_wait(k_full + s, (last[s] / kKStages) & 1, kWaitNs);
             }
@@ -276,10 +288,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (i >= kVStages &&
                     !tc::mbar_wait_abortable(v_empty + s, ((i / kVStages) - 1) & 1, kWaitNs, abort))
                     break;
-                tc::mbar_expect_tx(v_full + s, Lay::vBytes);
+                tc::mbar_expect_tx(v_full + s, Lay::vLoadBytes);
                 uint8_t *vd = sm + Lay::v0 + s * Lay::vBytes;
                 for (int c = 0; c < 2; ++c)
-                    tc::tma_load_3d(vd + c * (D * 128), &tm_v, i * kTile + c * 64, 0, bh, v_full + s);
+                    tc::tma_load_3d(vd + c * (Lay::vRows * 128), &tm_v, i * kTile + c * 64, 0, bh, v_full + s);
                 last[s] = i;
             }
             if (*abort) {
@@ -289,12 +301,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // -------------------------------------------------------- MMA issuer
-        // S_i = Q K_i^T runs up to two tiles ahead of the softmax (three S
-        // buffers); S_{i+3} is issued after PV_i, which read P_i from that
-        // buffer (the tensor pipe runs in order).
+        // S_i = Q K_i^T runs a tile ahead of the softmax (two S buffers);
+        // S_{i+2} is issued after PV_i, which read P_i from that buffer (the
+        // tensor pipe runs in order).  Both products take their A operand
+        // (Q, P) from tensor memory and only B (K, V) from shared memory.
         if (lane == 0) {
-            constexpr uint32_t idS = tc::idesc_f16_f32(kTile, kTile), idO = tc::idesc_f16_f32(kTile, D);
-            const uint32_t aq = tc::smem_u32(sm + Lay::q);
+            constexpr uint32_t idS = tc::idesc_f16_f32(kTile, kTile), idO = tc::idesc_f16_f32(kTile, Lay::vRows);
             bool ok = tc::mbar_wait_abortable(q_full, 0, kWaitNs, abort);
             int nq = 0;                        // next S product to issue
             for (int pv = 0; ok && pv < ntk; ++pv) {
@@ -305,8 +317,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const uint32_t ak = tc::smem_u32(sm + Lay::k0 + ks * Lay::kBytes);
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k)
-                        tc::mma_f16(tS0 + sb * kTile, tc::sw128_desc_k(aq, k, kTile),
-                                    tc::sw128_desc_k(ak, k, kTile), idS, k > 0);
+                        tc::mma_f16_ts(tS0 + sb * kTile, tQ + k * 8, tc::sw128_desc_k(ak, k, kTile), idS, k > 0);
                     tc::mma_commit(s_full + sb);
                     tc::mma_commit(k_empty + ks);
                 }
@@ -320,7 +331,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const uint32_t av = tc::smem_u32(sm + Lay::v0 + vs * Lay::vBytes);
 #pragma unroll
                 for (int k = 0; k < kTile / 16; ++k)
-                    tc::mma_f16_ts(tO, tS0 + sb * kTile + k * 8, tc::sw128_desc_k(av, k, D), idO,
+                    tc::mma_f16_ts(tO, tS0 + sb * kTile + k * 8, tc::sw128_desc_k(av, k, Lay::vRows), idO,
                                    (pv > 0 || k > 0) ? 1u : 0u);
                 tc::mma_commit(o_done + (pv & 1));
                 tc::mma_commit(v_empty + vs);
@@ -335,12 +346,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int t = t0 + row;
         const float qa = t < n ? a.qs[(size_t)bh * a.wq + t / a.gq] * a.scale_log2 : 0.0f;
         const float *ksr = a.ks + (size_t)bh * a.wk;
-        float *red = reinterpret_cast<float *>(sm + Lay::red);   // [3][2 halves][128 rows]
+        float *red = reinterpret_cast<float *>(sm + Lay::red);   // [2][2 halves][128 rows]
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        constexpr int OC = D / 32;             // 32-column chunks of O
+        constexpr int OC = (D + 32) / 32;      // 32-column chunks of O, the sum column included
         constexpr int OC0 = (OC + 1) / 2;      // chunks [0, OC0) rescaled by half 0, the rest by half 1
+        // Q (widened, fp16) into tensor memory: row t -> lane, element pairs
+        // -> consecutive columns; half 0 of each row writes it
+        if (g == 0) {
+            const uint4 *qrow = reinterpret_cast<const uint4 *>(a.q16 + ((size_t)bh * a.T + t) * D);
+#pragma unroll
+            for (int cq = 0; cq < D / 64; ++cq) {
+                uint32_t r[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint4 w = qrow[cq * 8 + e];
+                    r[4 * e] = w.x;
+                    r[4 * e + 1] = w.y;
+                    r[4 * e + 2] = w.z;
+                    r[4 * e + 3] = w.w;
+                }
+                tc::tmem_st32u(tQ + lane_base + cq * 32, r);
+            }
+            tc::tmem_st_wait();
+            tc::fence_before_sync();
+            tc::mbar_arrive(q_full);
+        }
         float m_use = -INFINITY;
-        uint64_t l2 = f2pack(0.0f, 0.0f);     // this half's weight sum, in two lanes
         bool ok = true, bad = false;
         // a warp-uniform outcome, so the warp-wide TMEM accesses stay converged
         auto wait_warp = [&](uint64_t *bar, uint32_t parity) {
@@ -402,7 +433,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (grow) {
                 alpha = ex2(m_use - mt);                   // 0 on the first tile
                 m_use = mt;
-                l2 = f2mul(l2, f2pack(alpha, alpha));
             }
             const float nm = -m_use;
             uint32_t pk[32];
@@ -414,9 +444,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int e = 0; e < 32; ++e) {
                     float y0, y1;
                     f2unpack(f2fma(f2pack(x[2 * e], x[2 * e + 1]), c2, nm2), y0, y1);
-                    const float p0 = ex2(y0), p1 = ex2(y1);
-                    l2 = f2add(l2, f2pack(p0, p1));
-                    const __half2 hp = __floats2half2_rn(p0, p1);
+                    const __half2 hp = __floats2half2_rn(ex2(y0), ex2(y1));
                     pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
             } else {
@@ -424,7 +452,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int e = 0; e < 32; ++e) {
                     const float p0 = 2 * e < nvalid ? ex2(fmaf(x[2 * e], c, nm)) : 0.0f;
                     const float p1 = 2 * e + 1 < nvalid ? ex2(fmaf(x[2 * e + 1], c, nm)) : 0.0f;
-                    l2 = f2add(l2, f2pack(p0, p1));
                     const __half2 hp = __floats2half2_rn(p0, p1);
                     pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
@@ -434,9 +461,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc::tmem_st32u(tS0 + sb * kTile + lane_base + g * 32, pk);
             tc::tmem_st_wait();
             // O *= alpha where the max grew: O must first hold PV_{i-1}.
-            // PV products alternate between two barriers; S_i completed after
-            // PV_{i-3}, so barrier (i-1) & 1 has completed either the phase
-            // waited for or the one before it, and the parity cannot alias.
+            // PV products alternate between two barriers; S_i was issued
+            // after PV_{i-2} and has completed, so barrier (i-1) & 1 has
+            // completed either the phase waited for or the one before it, and
+            // the parity cannot alias.
             if (i >= 1 && __any_sync(0xffffffffu, grow)) {
                 bad = !wait_warp(o_done + ((i - 1) & 1), ((i - 1) >> 1) & 1);
                 if (bad) continue;             // the next barrier takes everyone out
@@ -455,14 +483,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc::fence_before_sync();
             tc::mbar_arrive(p_ready + sb);
         }
-        // the two halves' sums meet (every softmax thread reaches this point)
-        float l0, l1;
-        f2unpack(l2, l0, l1);
-        red[(4 + g) * kTile + row] = l0 + l1;
-        const bool fine = !tc::bar_or(1, kSoftmaxThreads, !ok || bad || *abort);
-        const float inv_l = 1.0f / (red[4 * kTile + row] + red[5 * kTile + row]);
-        if (fine && wait_warp(o_last, 0)) {
+        if (ok && !bad && wait_warp(o_last, 0)) {
             tc::fence_after_sync();
+            float inv_l;
+            {
+                float v[32];
+                tc::tmem_ld32(tO + lane_base + D, v);      // column D: the sum of the weights
+                inv_l = 1.0f / v[0];
+            }
             const float *vsc = a.vs + (size_t)bh * D;
             const size_t orow = (((size_t)b * n + t) * a.h + j) * D;
 #pragma unroll
@@ -599,8 +627,7 @@ extern "C" int ulp_sage_attention(const int8_t *q8, const int8_t *k8, const uint
     const size_t plane = (size_t)B * h * T * D;
     uint16_t *q16 = reinterpret_cast<uint16_t *>(workspace), *k16 = q16 + plane, *v16 = k16 + plane;
 
-    CUtensorMap mq, mk, mv;
-    if (int s = make_map(&mq, q16, D, T, (uint64_t)B * h, kTile)) return s;
+    CUtensorMap mk, mv;
     if (int s = make_map(&mk, k16, D, T, (uint64_t)B * h, kTile)) return s;
     if (int s = make_map(&mv, v16, T, D, (uint64_t)B * h, D)) return s;
 
@@ -618,6 +645,8 @@ extern "C" int ulp_sage_attention(const int8_t *q8, const int8_t *k8, const uint
     a.wq = (n + q_group - 1) / q_group;
     a.wk = (n + kGK - 1) / kGK;
     a.ntk = T / kTile;
+    a.T = T;
+    a.q16 = q16;
     a.scale_log2 = sm_scale * 1.4426950408889634f;
     const dim3 grid((unsigned)a.ntk, (unsigned)h, (unsigned)B);
     // one CTA per SM (it holds all 512 TMEM columns): at D = 64 the request
@@ -625,11 +654,11 @@ extern "C" int ulp_sage_attention(const int8_t *q8, const int8_t *k8, const uint
     if (D == 128) {
         const size_t bytes = AttnLayout<128>::bytes + 1024;
         cudaFuncSetAttribute(sage_attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-        sage_attention_kernel<128><<<grid, kAttnThreads, bytes, st>>>(mq, mk, mv, a);
+        sage_attention_kernel<128><<<grid, kAttnThreads, bytes, st>>>(mk, mv, a);
     } else {
         const size_t bytes = std::max<size_t>(AttnLayout<64>::bytes + 1024, 120 * 1024);
         cudaFuncSetAttribute(sage_attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-        sage_attention_kernel<64><<<grid, kAttnThreads, bytes, st>>>(mq, mk, mv, a);
+        sage_attention_kernel<64><<<grid, kAttnThreads, bytes, st>>>(mk, mv, a);
     }
     return check_launch("sage_attention");
 }

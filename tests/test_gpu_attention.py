@@ -12,15 +12,15 @@ Vmax = max over the live keys of |V[u, d]| for that batch, head and channel):
     is off by at most ln2 * 6 * 2^-24 * xmax relative, plus the 2^-22 of the
     hardware exp2;
   * each weight is rounded to fp16 (2^-11 relative in the normal range,
-    2^-25 absolute below it) for the numerator, so the output is a weighted
-    mean with weights perturbed by eps_w = 2^-11 + 6 ln2 2^-24 xmax + 2^-22
-    relative: error <= 2 eps_w Vmax, plus n 2^-25 Vmax for the subnormal
-    weights; the denominator sums the unrounded weights, which scales the
-    result by a factor within 2^-11 of 1: another 2^-11 Vmax;
+    2^-25 absolute below it) and the denominator sums the rounded weights, so
+    the output is a weighted mean with weights perturbed by
+    eps_w = 2^-11 + 6 ln2 2^-24 xmax + 2^-22 relative: error <= 2 eps_w Vmax,
+    plus n 2^-25 Vmax for the subnormal weights;
   * fp32 accumulation of the n products in the PV MMAs and the O rescales,
-    and of the denominator: <= 2 (n + ntiles) 2^-23 Vmax; the final scaling
-    by 1/l and v_scale: 3 2^-24.
-bound(n, xmax) = 2 eps_w + 2^-11 + n (2^-22 + 2^-25) + (2 ceil(n/128) + 3) 2^-23.
+    for the numerator and (through a row of ones in V) the denominator alike:
+    <= 2 (n + ntiles) 2^-23 Vmax; the final scaling by 1/l and v_scale:
+    3 2^-24.
+bound(n, xmax) = 2 eps_w + n (2^-22 + 2^-25) + (2 ceil(n/128) + 3) 2^-23.
 bf16 / fp16 outputs add one rounding of the result (2^-9 / 2^-12 relative).
 """
 import math
@@ -39,8 +39,7 @@ pytestmark = pytest.mark.gpu
 
 def bound(n: int, xmax: float) -> float:
     eps_w = 2.0 ** -11 + 6 * math.log(2) * 2.0 ** -24 * xmax + 2.0 ** -22
-    return (2 * eps_w + 2.0 ** -11 + n * (2.0 ** -22 + 2.0 ** -25)
-            + (2 * math.ceil(n / 128) + 3) * 2.0 ** -23)
+    return 2 * eps_w + n * (2.0 ** -22 + 2.0 ** -25) + (2 * math.ceil(n / 128) + 3) * 2.0 ** -23
 
 
 def extent(c, sm_scale=None):
