@@ -438,13 +438,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             uint32_t pk[32];
             if (nvalid == 64) {
                 // exponents two at a time (packed fma.rn.f32x2: the same
-                // rounding as two fmaf)
+                // rounding as two fmaf); three passes over the 64 values
+                // (exponents, exp2, fp16 pairs) keep 64 independent
+                // operations in flight per step
                 const uint64_t c2 = f2pack(c, c), nm2 = f2pack(nm, nm);
 #pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    f2unpack(f2fma(f2pack(x[2 * e], x[2 * e + 1]), c2, nm2), x[2 * e], x[2 * e + 1]);
+#pragma unroll
+                for (int e = 0; e < 64; ++e) x[e] = ex2(x[e]);
+#pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    float y0, y1;
-                    f2unpack(f2fma(f2pack(x[2 * e], x[2 * e + 1]), c2, nm2), y0, y1);
-                    const __half2 hp = __floats2half2_rn(ex2(y0), ex2(y1));
+                    const __half2 hp = __floats2half2_rn(x[2 * e], x[2 * e + 1]);
                     pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
             } else {
