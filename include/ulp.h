@@ -121,7 +121,8 @@ int ulp_chunk_bytes(int B, int L, int h, int D, int q_group, size_t *chunk_bytes
  * q_scale, k_scale. */
 int ulp_chunk_offsets(int B, int L, int h, int D, int q_group, size_t offsets[5]);
 
-/* Bytes of the workspace ulp_k_mean_global needs: 8 * P * B * ceil(L/512) * H * D. */
+/* Bytes of the workspace ulp_k_mean_global needs: 8 * P * B * ceil(L/64) * H * D
+ * (one fp64 tree node per 64-row block: the bound for every launch shape). */
 int ulp_k_mean_workspace_bytes(int B, int L, int H, int D, int world_size, size_t *bytes);
 
 /* k_mean_global production for an emulated Ulysses group (the global K mean
@@ -139,10 +140,21 @@ int ulp_k_mean_workspace_bytes(int B, int L, int H, int D, int world_size, size_
  *   workspace  device buffer of at least ulp_k_mean_workspace_bytes bytes
  *              (holds tree nodes; contents on return unspecified)
  *   k_mean     [B, H, D] dtype (output)
- * local_sequence is at most 32768 (ULP_EINVAL above). */
+ * local_sequence is at most 262144 (ULP_EINVAL above). */
 int ulp_k_mean_global(const void *k, int dtype, int B, int L, int H, int D, int world_size,
                       int used_sequence, void *workspace, size_t workspace_bytes, void *k_mean,
                       ulp_stream_t stream);
+
+/* ulp_k_mean_global with the launch shape fixed: each thread of the first
+ * kernel sums blocks_per_thread (1, 2, 4 or 8) consecutive 64-row blocks and
+ * the lowest tree levels over them.  ulp_k_mean_global picks this number from
+ * the shape and the device; every value gives the same bits (the summation
+ * order above does not depend on it).  The pages have no counterpart; it
+ * exists so that tests can check that every launch shape agrees.  ULP_EINVAL
+ * for other values. */
+int ulp_k_mean_global_grouped(const void *k, int dtype, int B, int L, int H, int D, int world_size,
+                              int used_sequence, int blocks_per_thread, void *workspace,
+                              size_t workspace_bytes, void *k_mean, ulp_stream_t stream);
 
 /* ulp_k_mean_global without a workspace.  The pages have no counterpart of
  * this entry point; it exists for callers that cannot allocate device memory

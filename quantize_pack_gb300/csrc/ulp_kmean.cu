@@ -8,30 +8,32 @@
 //               power of two, adjacent pairs level by level): the rank's
 //               all-reduce contribution; total = fp64 sum over ranks in order;
 //   mean      = binary32 rounding of total / used, then the dtype (RNE).
-// Kernel A: a thread sums 8 consecutive blocks of 8 channels and the three
-// lowest tree levels over them, writing one fp64 node per group of 8 blocks
-// to the workspace; kernel B (one thread per channel) finishes each rank's
-// tree and the rank sum.  Reads 2 bytes per K element: HBM-bound.
+// Kernel A: a thread sums G consecutive blocks (G = 1, 2, 4 or 8, chosen
+// from the shape so the grid fills whole waves) of 4 channels and the log2 G
+// lowest tree levels over them, writing one fp64 node per group of G blocks
+// to the workspace; kernel B (one thread per rank and channel) finishes each
+// rank's tree and the rank sum.  Reads 2 bytes per K element: HBM-bound.
 #include "ulp_internal.cuh"
 
 namespace ulp {
 
 constexpr int kMeanBlock = 64;        // rows per block sum
-constexpr int kMeanGroup = 8;         // blocks per kernel-A thread (3 tree levels)
-static_assert(kMeanGroup == 8, "kernel A builds exactly three tree levels");
 constexpr int kMeanThreads = 128;
+constexpr int kMeanMaxNodes = 512;    // tree leaves kernel B accepts per rank (9 levels)
 
 struct KMeanArgs {
     const uint16_t *k;   // [P, B, L, H, D]
-    double *nodes;       // [P, B, ngrp, H, D]: tree nodes over 8 blocks each
+    double *nodes;       // [P, B, ngrp, H, D]: tree nodes over G blocks each
     void *out;           // [B, H, D] dtype
     int B, L, H, D, P, nblk, ngrp, used, dtype;
 };
 
 // Kernel A: grid (ceil(H*D/4 / 128), ngrp, P * B); a thread owns 4 channels.
-template <int DT>
+template <int DT, int G>
 __global__ void __launch_bounds__(kMeanThreads) kmean_blocks_kernel(KMeanArgs a)
 {
+    static_assert(G == 1 || G == 2 || G == 4 || G == 8, "blocks per thread");
+    constexpr int LV = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;   // in-thread tree levels
     pdl_trigger();
     pdl_wait();
     const int HD = a.H * a.D;
@@ -41,14 +43,15 @@ __global__ void __launch_bounds__(kMeanThreads) kmean_blocks_kernel(KMeanArgs a)
     const int r = blockIdx.z / a.B, b = blockIdx.z - r * a.B;
     const int row_live = max(0, a.used - r * a.L);               // rank-local rows < this are live
     const uint16_t *src = a.k + ((size_t)r * a.B + b) * a.L * HD + (size_t)vec * 4;
-    // The three lowest levels of the rank's pairwise tree, built as the blocks
-    // arrive: a carry stack of left children per level (lv1 holds a finished
-    // pair, lv2 a finished quad), each node = left child + right child.
+    // The lowest levels of the rank's pairwise tree, built as the blocks
+    // arrive: lv0 holds a finished block sum waiting for its right sibling
+    // (fp32), st[l] a finished level-l node waiting for its sibling (fp64);
+    // each node = left child + right child.
     float lv0[4];
-    double lv1[4], lv2[4], top[4];
+    double st[LV > 1 ? LV - 1 : 1][4], top[4];
 #pragma unroll 1
-    for (int q = 0; q < kMeanGroup; ++q) {
-        const int t0 = (grp * kMeanGroup + q) * kMeanBlock;
+    for (int q = 0; q < G; ++q) {
+        const int t0 = (grp * G + q) * kMeanBlock;
         const int t1 = min(min(t0 + kMeanBlock, a.L), row_live);
         float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         for (int t = t0; t < t1; t += 16) {
@@ -67,27 +70,34 @@ __global__ void __launch_bounds__(kMeanThreads) kmean_blocks_kernel(KMeanArgs a)
                 }
             }
         }
-        if (!(q & 1)) {
+        if (LV == 0) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) top[x] = (double)s[x];
+        } else if (!(q & 1)) {
 #pragma unroll
             for (int x = 0; x < 4; ++x) lv0[x] = s[x];
         } else {
-            double pair[4];
+            double node[4];
 #pragma unroll
-            for (int x = 0; x < 4; ++x) pair[x] = __dadd_rn((double)lv0[x], (double)s[x]);
-            if (!(q & 2)) {
+            for (int x = 0; x < 4; ++x) node[x] = __dadd_rn((double)lv0[x], (double)s[x]);
+            // node is at level 1; merge with finished left siblings above it
+            bool done = false;
 #pragma unroll
-                for (int x = 0; x < 4; ++x) lv1[x] = pair[x];
-            } else {
-                double quad[4];
+            for (int l = 1; l < LV; ++l) {
+                if (!done) {
+                    if (!((q >> l) & 1)) {
 #pragma unroll
-                for (int x = 0; x < 4; ++x) quad[x] = __dadd_rn(lv1[x], pair[x]);
-                if (!(q & 4)) {
+                        for (int x = 0; x < 4; ++x) st[l - 1][x] = node[x];
+                        done = true;
+                    } else {
 #pragma unroll
-                    for (int x = 0; x < 4; ++x) lv2[x] = quad[x];
-                } else {
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) top[x] = __dadd_rn(lv2[x], quad[x]);
+                        for (int x = 0; x < 4; ++x) node[x] = __dadd_rn(st[l - 1][x], node[x]);
+                    }
                 }
+            }
+            if (q == G - 1) {
+#pragma unroll
+                for (int x = 0; x < 4; ++x) top[x] = node[x];
             }
         }
     }
@@ -113,24 +123,34 @@ __global__ void __launch_bounds__(256) kmean_finish_kernel(KMeanArgs a)
     const int b = live ? (int)(idx / HD) : 0, ch = live ? (int)(idx - (long long)b * HD) : 0;
     int n2 = 1;
     while (n2 < a.ngrp) n2 *= 2;
-    double st[6];                                      // carry stack, n2 <= 64 (checked on the host)
+    double st[9];                                      // carry stack, n2 <= 512 (checked on the host)
 #pragma unroll
-    for (int l = 0; l < 6; ++l) st[l] = 0.0;
+    for (int l = 0; l < 9; ++l) st[l] = 0.0;
     double root = 0.0;
     if (live) {
         const double *col = a.nodes + (((size_t)r * a.B + b) * a.ngrp) * HD + ch;
-        for (int i = 0; i < n2; ++i) {
-            double x = i < a.ngrp ? col[(size_t)i * HD] : 0.0;
-            // x is a node at level 0; merge with finished left siblings
+        // eight nodes loaded ahead of their additions
+        for (int i0 = 0; i0 < n2; i0 += 8) {
+            double xs[8];
 #pragma unroll
-            for (int l = 0; l < 6; ++l) {
-                if (!((i >> l) & 1)) {
-                    st[l] = x;                         // a left child waits at level l
-                    break;
+            for (int u = 0; u < 8; ++u) xs[u] = i0 + u < a.ngrp ? col[(size_t)(i0 + u) * HD] : 0.0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u;
+                if (i < n2) {
+                    double x = xs[u];
+                    // x is a node at level 0; merge with finished left siblings
+#pragma unroll
+                    for (int l = 0; l < 9; ++l) {
+                        if (!((i >> l) & 1)) {
+                            st[l] = x;                 // a left child waits at level l
+                            break;
+                        }
+                        x = __dadd_rn(st[l], x);       // left + right
+                    }
+                    if (i == n2 - 1) root = x;     // the last leaf completes the tree
                 }
-                x = __dadd_rn(st[l], x);               // left + right
             }
-            if (i == n2 - 1) root = x;             // the last leaf completes the tree
         }
     }
     part[r][c] = root;
@@ -152,27 +172,79 @@ int kmean_check(int dtype, int B, int L, int H, int D, int world_size, int used_
     return ULP_OK;
 }
 
-static int kmean_groups(int L)
-{
-    const int nblk = (L + kMeanBlock - 1) / kMeanBlock;
-    return (nblk + kMeanGroup - 1) / kMeanGroup;
-}
+static int kmean_blocks(int L) { return (L + kMeanBlock - 1) / kMeanBlock; }
+static int kmean_groups(int L, int G) { return (kmean_blocks(L) + G - 1) / G; }
 
+// Tree nodes for the smallest group (G = 1), which bounds every G.
 size_t kmean_workspace_bytes(int B, int L, int H, int D, int world_size)
 {
-    return sizeof(double) * (size_t)world_size * B * kmean_groups(L) * H * D;
+    return sizeof(double) * (size_t)world_size * B * kmean_groups(L, 1) * H * D;
 }
 
-// Both launches on `stream`; `blocks` holds kmean_workspace_bytes bytes.
-int kmean_launch(const void *k, int dtype, int B, int L, int H, int D, int world_size,
-                 int used_sequence, double *nodes, void *k_mean, cudaStream_t stream)
+template <int DT>
+static void launch_blocks(int G, dim3 grid, cudaStream_t st, const KMeanArgs &a)
 {
-    KMeanArgs a{(const uint16_t *)k, nodes, k_mean, B, L, H, D, world_size,
-                (L + kMeanBlock - 1) / kMeanBlock, kmean_groups(L),
-                used_sequence < 0 ? L * world_size : used_sequence, dtype};
-    if (a.ngrp > 64)
-        return fail(ULP_EINVAL, "k_mean_global: local_sequence %d above the %d-row maximum", L,
-                    64 * kMeanGroup * kMeanBlock);
+    if (G == 1) launch_kernel(kmean_blocks_kernel<DT, 1>, grid, dim3(kMeanThreads), st, false, a);
+    else if (G == 2) launch_kernel(kmean_blocks_kernel<DT, 2>, grid, dim3(kMeanThreads), st, false, a);
+    else if (G == 4) launch_kernel(kmean_blocks_kernel<DT, 4>, grid, dim3(kMeanThreads), st, false, a);
+    else launch_kernel(kmean_blocks_kernel<DT, 8>, grid, dim3(kMeanThreads), st, false, a);
+}
+
+// Resident kernel-A CTAs per SM for group G (cached per device and dtype).
+static int resident_ctas(int G, int dtype)
+{
+    static int cache[64][2][4];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3, di = dtype == ULP_BF16 ? 0 : 1;
+    int &c = cache[dev][di][gi];
+    if (c == 0) {
+        int n = 0;
+        const void *f = nullptr;
+        if (dtype == ULP_BF16)
+            f = G == 1 ? (const void *)kmean_blocks_kernel<ULP_BF16, 1> : G == 2 ? (const void *)kmean_blocks_kernel<ULP_BF16, 2>
+              : G == 4 ? (const void *)kmean_blocks_kernel<ULP_BF16, 4> : (const void *)kmean_blocks_kernel<ULP_BF16, 8>;
+        else
+            f = G == 1 ? (const void *)kmean_blocks_kernel<ULP_FP16, 1> : G == 2 ? (const void *)kmean_blocks_kernel<ULP_FP16, 2>
+              : G == 4 ? (const void *)kmean_blocks_kernel<ULP_FP16, 4> : (const void *)kmean_blocks_kernel<ULP_FP16, 8>;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kMeanThreads, 0) != cudaSuccess || n < 1) n = 1;
+        c = n;
+    }
+    return c;
+}
+
+// Blocks per kernel-A thread: the largest G whose grid fills its waves best
+// (the fraction of the last wave in use), among the G that keep kernel B's
+// tree within kMeanMaxNodes leaves.  Every G gives the same bits.
+static int choose_group(int L, int H, int D, int P, int B, int dtype)
+{
+    int sms = 148, dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long gx = ((long long)H * D / 4 + kMeanThreads - 1) / kMeanThreads;
+    int best = 8;
+    double best_eff = -1.0;
+    for (int G = 8; G >= 1; G /= 2) {
+        if (kmean_groups(L, G) > kMeanMaxNodes) break;
+        const double ctas = (double)gx * kmean_groups(L, G) * P * B;
+        const double waves = ctas / ((double)resident_ctas(G, dtype) * sms);
+        const double eff = waves / ceil(waves);
+        if (eff > best_eff + 0.02) {               // a smaller G must fill clearly better
+            best_eff = eff;
+            best = G;
+        }
+    }
+    return best;
+}
+
+// Both launches on `stream`; `nodes` holds the tree nodes for group size G.
+int kmean_launch(const void *k, int dtype, int B, int L, int H, int D, int world_size,
+                 int used_sequence, int G, double *nodes, void *k_mean, cudaStream_t stream)
+{
+    KMeanArgs a{(const uint16_t *)k, nodes, k_mean, B, L, H, D, world_size, kmean_blocks(L),
+                kmean_groups(L, G), used_sequence < 0 ? L * world_size : used_sequence, dtype};
+    if (a.ngrp > kMeanMaxNodes)
+        return fail(ULP_EINVAL, "k_mean_global: local_sequence %d above the %d-row maximum for this group size", L,
+                    kMeanMaxNodes * G * kMeanBlock);
     const long long vecs = (long long)H * D / 4;
     const long long gx = (vecs + kMeanThreads - 1) / kMeanThreads;
     if (gx > INT_MAX || (long long)world_size * B > 65535)
@@ -181,10 +253,10 @@ int kmean_launch(const void *k, int dtype, int B, int L, int H, int D, int world
     const long long nb = ((long long)B * H * D + 31) / 32;
     if (nb > INT_MAX) return fail(ULP_EINVAL, "k_mean_global: grid too large");
     if (dtype == ULP_BF16) {
-        launch_kernel(kmean_blocks_kernel<ULP_BF16>, grid_a, dim3(kMeanThreads), stream, false, a);
+        launch_blocks<ULP_BF16>(G, grid_a, stream, a);
         launch_kernel(kmean_finish_kernel<ULP_BF16>, dim3((unsigned)nb), dim3(32 * world_size), stream, false, a);
     } else {
-        launch_kernel(kmean_blocks_kernel<ULP_FP16>, grid_a, dim3(kMeanThreads), stream, false, a);
+        launch_blocks<ULP_FP16>(G, grid_a, stream, a);
         launch_kernel(kmean_finish_kernel<ULP_FP16>, dim3((unsigned)nb), dim3(32 * world_size), stream, false, a);
     }
     return check_launch("k_mean_global");
@@ -215,7 +287,25 @@ int ulp_k_mean_global(const void *k, int dtype, int B, int L, int H, int D, int 
     const size_t need = kmean_workspace_bytes(B, L, H, D, world_size);
     if (workspace_bytes < need)
         return fail(ULP_EINVAL, "k_mean_global: workspace of %zu bytes, %zu needed", workspace_bytes, need);
-    return kmean_launch(k, dtype, B, L, H, D, world_size, used_sequence, (double *)workspace, k_mean,
+    const int G = choose_group(L, H, D, world_size, B, dtype);
+    return kmean_launch(k, dtype, B, L, H, D, world_size, used_sequence, G, (double *)workspace, k_mean,
+                        (cudaStream_t)stream);
+}
+
+int ulp_k_mean_global_grouped(const void *k, int dtype, int B, int L, int H, int D, int world_size,
+                              int used_sequence, int blocks_per_thread, void *workspace,
+                              size_t workspace_bytes, void *k_mean, ulp_stream_t stream)
+{
+    if (int s = kmean_check(dtype, B, L, H, D, world_size, used_sequence)) return s;
+    const int G = blocks_per_thread;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(ULP_EINVAL, "k_mean_global_grouped: blocks_per_thread must be 1, 2, 4 or 8 (got %d)", G);
+    if (!aligned16(k) || !aligned16(workspace) || !aligned16(k_mean))
+        return fail(ULP_EALIGN, "k_mean_global: k, workspace, k_mean must be 16-byte aligned");
+    const size_t need = kmean_workspace_bytes(B, L, H, D, world_size);
+    if (workspace_bytes < need)
+        return fail(ULP_EINVAL, "k_mean_global: workspace of %zu bytes, %zu needed", workspace_bytes, need);
+    return kmean_launch(k, dtype, B, L, H, D, world_size, used_sequence, G, (double *)workspace, k_mean,
                         (cudaStream_t)stream);
 }
 
@@ -272,7 +362,8 @@ extern "C" int ulp_k_mean_global_noalloc(const void *k, int dtype, int B, int L,
     if (int s = kmean_check(dtype, B, L, H, D, world_size, used_sequence)) return s;
     if (!aligned16(k) || !aligned16(k_mean))
         return fail(ULP_EALIGN, "k_mean_global_noalloc: k and k_mean must be 16-byte aligned");
-    const size_t need = kmean_workspace_bytes(B, L, H, D, world_size);
+    // groups of 8 blocks: the smallest node array (8 * P * B * ceil(L/512) * H * D bytes)
+    const size_t need = sizeof(double) * (size_t)world_size * B * ((L + 511) / 512) * H * D;
     if (need > kNoAllocScratchBytes)
         return fail(ULP_EINVAL,
                     "k_mean_global_noalloc: this shape needs %zu bytes of scratch, the fixed "
@@ -282,6 +373,6 @@ extern "C" int ulp_k_mean_global_noalloc(const void *k, int dtype, int B, int L,
     if (int s = scratch_address(&scratch)) return s;
     // Every tree node kernel B reads is written by kernel A of the same call,
     // so the previous call's leftovers never need clearing.
-    return kmean_launch(k, dtype, B, L, H, D, world_size, used_sequence, (double *)scratch, k_mean,
+    return kmean_launch(k, dtype, B, L, H, D, world_size, used_sequence, 8, (double *)scratch, k_mean,
                         (cudaStream_t)stream);
 }

@@ -60,6 +60,7 @@ def lib() -> ctypes.CDLL:
         L.ulp_k_mean_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]
         L.ulp_k_mean_global.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _P]
         L.ulp_k_mean_global_noalloc.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P]
+        L.ulp_k_mean_global_grouped.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _P]
         L.ulp_k_grouped_amax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P]
         L.ulp_boundary_minmax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]
         L.ulp_derive_k_boundary_amax.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]
@@ -73,6 +74,7 @@ def lib() -> ctypes.CDLL:
         L.ulp_sage_attention_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]
         for name in ("ulp_slots", "ulp_scale_widths", "ulp_chunk_bytes", "ulp_chunk_offsets",
                      "ulp_k_mean_workspace_bytes", "ulp_k_mean_global", "ulp_k_mean_global_noalloc",
+                     "ulp_k_mean_global_grouped",
                      "ulp_k_grouped_amax", "ulp_boundary_minmax", "ulp_derive_k_boundary_amax",
                      "ulp_pack", "ulp_alltoall_emulate", "ulp_unpack_for_sage",
                      "ulp_sage_attention", "ulp_sage_attention_workspace_bytes"):
@@ -185,6 +187,27 @@ def k_mean_global(k: torch.Tensor, *, used_sequence: Optional[int] = None,
     _check(lib().ulp_k_mean_global(_ptr(k), _dtype_code(k), B, L, H, D, P, _opt(used_sequence),
                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _ptr(out), _stream(k.device)))
+    return out
+
+
+def k_mean_global_grouped(k: torch.Tensor, blocks_per_thread: int, *,
+                          used_sequence: Optional[int] = None,
+                          workspace: Optional[torch.Tensor] = None,
+                          out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """k_mean_global with the first kernel's blocks per thread fixed (1, 2, 4
+    or 8) instead of chosen from the shape; the bits are the same for every
+    value."""
+    P, B, L, H, D = k.shape
+    if workspace is None:
+        workspace = torch.empty(k_mean_workspace_bytes(B, L, H, D, P), dtype=torch.uint8,
+                                device=k.device)
+    if out is None:
+        out = torch.empty((B, H, D), dtype=k.dtype, device=k.device)
+    _check(lib().ulp_k_mean_global_grouped(_ptr(k), _dtype_code(k), B, L, H, D, P,
+                                           _opt(used_sequence), int(blocks_per_thread),
+                                           _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(),
+                                           _ptr(out), _stream(k.device)))
     return out
 
 
