@@ -15,7 +15,7 @@
 namespace ulp {
 
 constexpr int kUnpackThreads = 128;
-constexpr int kCopyVecPerThread = 8;
+constexpr int kCopyVecPerThread = 16;
 constexpr int kCopyPiece = kUnpackThreads * kCopyVecPerThread * 16;   // bytes per copy block
 
 struct UnpackArgs {
