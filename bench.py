@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--mode", choices=["fused", "unfused"], default="fused")
     ap.add_argument("--q-group", type=int, choices=[64, 128], default=128,
                     help="Q group rows (64: Q groups are the K groups)")
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum CPU time spent on the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
