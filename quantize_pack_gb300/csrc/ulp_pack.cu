@@ -11,9 +11,9 @@
 // registers.
 // Boundary groups (the rank's first/last touched group) take their amax from
 // the gathered partials (Q) or the derived slots (K), so every input byte
-// crosses HBM once.  Quotients use a correctly rounded reciprocal with an
-// exact fallback near rounding boundaries (ulp_internal.cuh), so the codes are
-// those of the IEEE quotient.
+// crosses HBM once.  Quotients use a correctly rounded reciprocal and
+// Markstein's correction (ulp_internal.cuh), so the codes are those of the
+// IEEE quotient.
 #include "ulp_internal.cuh"
 
 namespace ulp {
