@@ -10,38 +10,36 @@
 // 128^3 = 2^21 the integer dot products accumulate exactly in fp32; E4M3 is a
 // subset of fp16, so V widens exactly too.  The per-group scales multiply the
 // integer logits in fp32.  P = exp2(x - m) is rounded to fp16 for the PV
-// product and the softmax denominator sums the same rounded values, so the
-// output is an exact weighted mean with weights perturbed by at most 2^-11
-// relative.  Scales must be positive (they are amax / 127).
+// product while the softmax denominator sums the fp32 weights, so rounding P
+// moves the output by at most 2^-11 of max |V|.  Scales must be positive
+// (they are amax / 127).
 //
 // Two kernels.  The widen pass writes Q and K as fp16 [B*h, T, D] and V as
 // fp16 [B*h, D, T] (T = the live prefix rounded up to 128 rows, zero past
 // it) into a workspace, once per call, so the attention kernel moves every
 // tile with TMA straight into the tensor core's 128-byte swizzled operand
-// layout.  The attention kernel runs one CTA of ten warps per (b, head,
-// 128-query tile):
-//   warps 8 and 10 (TMA): K tiles of 128 keys into three stages (a stage
-//     frees when its S product completes), V tiles into two stages (freed
-//     when the PV product completes);
-//   warp 9 (MMA, one thread): S_i = Q K_i^T into one of two TMEM buffers, a
-//     tile ahead of the softmax, and O += P_i V_i; Q and P are the A
-//     operands in tensor memory, so the products read only K and V from
-//     shared memory;
-//   warps 0-7 (softmax): query row = TMEM lane (warp % 4 picks the lane
-//     quarter), warps 0-3 take keys 0-63 of each tile and warps 4-7 keys
-//     64-127 (one K scale each); the two threads of a row exchange their
-//     maxima through shared memory.  They keep the running max m of the
-//     scaled logits and write P = 2^(S c - m) (fp16) into tensor memory over
-//     the S tile it came from; the PV product reads its A operand from
-//     there, so P needs neither shared memory nor a wait for the previous
-//     PV (the tensor pipe runs in order: QK_{i+2} overwrites that buffer
-//     only after PV_i has read it).  m moves only when the tile's max exceeds it by more
-//     than 8 (log2 units), so O is rescaled rarely; weights stay <= 2^8 and
-//     numerator and denominator share the same m, so this is exact algebra.
-//     The denominator is accumulated by the tensor core itself: each V tile
-//     carries a row of ones, so O's column D is the sum of the weights.
-// Every mbarrier wait is bounded: on a timeout the CTA records a status,
-// every role stops, the tensor memory is freed and nothing is written.
+// layout.  The attention kernel runs one CTA of eleven warps per (b, head,
+// pair of 128-query tiles A and B):
+//   warp 8 (TMA): the two Q tiles once, then K tiles of 128 keys into three
+//     stages (a stage frees when both S products that read it complete);
+//   warp 10 (TMA): V tiles into two stages (freed when both PV products
+//     that read them complete);
+//   warp 9 (MMA, one thread): per K tile i, O_A += P_A(i-1) V(i-1), then
+//     S_A(i) = Q_A K_i^T, then the same for B; P is the A operand in tensor
+//     memory, Q, K and V come from shared memory;
+//   warps 0-3 (softmax of tile A) and 4-7 (tile B): one query row per
+//     thread (TMEM lane = row), all 128 keys of each K tile.  A thread keeps
+//     its row's running max m of the scaled logits and the running sum l of
+//     the weights, and writes P = 2^(S c - m) (fp16) into tensor memory over
+//     the S tile it came from.  The tensor pipe runs in order, so S(i+1)
+//     overwrites that buffer only after PV(i) has read it, and the commit
+//     that completes S(i+1) also covers PV(i): when a warpgroup sees S(i+1)
+//     its O is settled and may be rescaled.  m moves only when the tile's
+//     max exceeds it by more than 8 (log2 units), so O is rescaled rarely;
+//     weights stay <= 2^8, and numerator and denominator share the same m.
+// Each K and V tile is read once for 256 queries.  Every mbarrier wait is
+// bounded: on a timeout the CTA records a status, every role stops, the
+// tensor memory is freed and nothing is written.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -56,13 +54,13 @@ namespace ulp {
 
 namespace {
 
-constexpr int kTile = 128;                 // queries per CTA, keys per step
+constexpr int kTile = 128;                 // queries per tile, keys per step
+constexpr int kQTiles = 2;                 // query tiles per CTA, one per softmax warpgroup
 constexpr int kSoftmaxThreads = 256;       // warps 0-7
-constexpr int kAttnThreads = 352;          // + K/Q TMA warp 8, MMA warp 9, V TMA warp 10
+constexpr int kAttnThreads = 352;          // + Q/K TMA warp 8, MMA warp 9, V TMA warp 10
 constexpr int kKTmaWarp = 8, kMmaWarp = 9, kVTmaWarp = 10;
-constexpr int kSBufs = 2;                  // S / P buffers in TMEM
 constexpr int kKStages = 3, kVStages = 2;  // shared-memory stages
-constexpr uint32_t kTmemCols = 512;        // S0, S1: 128 columns each; O: D + 16 (sum in column D); Q: D / 2
+constexpr uint32_t kTmemCols = 512;        // S_A, S_B: 128 columns each; O_A, O_B: D each
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr float kRescaleLog2 = 8.0f;       // max growth (log2) absorbed without rescaling O
 
@@ -152,29 +150,22 @@ __global__ void __launch_bounds__(256) attn_widen_kernel(WidenArgs a)
 // ------------------------------------------------------- attention kernel
 
 struct AttnArgs {
-    const uint16_t *q16;                   // widened Q [B*h, T, D]
     const float *qs, *ks, *vs;
     void *out;
     int *status;
     int out_dtype;
-    int h, n, gq, wq, wk, ntk, T;
+    int h, n, gq, wq, wk, ntk;
     float scale_log2;                      // sm_scale * log2(e)
 };
 
-// A V tile holds D channel rows and 16 more: a row of ones (so the PV product
-// also accumulates the softmax denominator, in O's column D) and 15 zero rows.
 template <int D>
 struct AttnLayout {
-    static constexpr int vRows = D + 16;
-    static constexpr uint32_t kBytes = kTile * D * 2;         // one K tile
-    static constexpr uint32_t vBytes = vRows * kTile * 2;     // one V tile
-    static constexpr uint32_t vLoadBytes = D * kTile * 2;     // what TMA writes of it
-    static constexpr uint32_t k0 = 0;                         // kKStages K tiles
-    static constexpr uint32_t v0 = k0 + kKStages * kBytes;    // kVStages V tiles
-    // softmax max exchange, fp32 [2][2][128]: even and odd tiles; [.][g][row]
-    // is written by half g
-    static constexpr uint32_t red = v0 + kVStages * vBytes;
-    static constexpr uint32_t bars = red + 4 * kTile * 4;
+    static constexpr uint32_t tBytes = kTile * D * 2;         // a Q or K tile: 128 rows x D
+    static constexpr uint32_t vBytes = D * kTile * 2;         // a V tile: D rows x 128 keys
+    static constexpr uint32_t q0 = 0;                         // kQTiles Q tiles
+    static constexpr uint32_t k0 = q0 + kQTiles * tBytes;     // kKStages K tiles
+    static constexpr uint32_t v0 = k0 + kKStages * tBytes;    // kVStages V tiles
+    static constexpr uint32_t bars = v0 + kVStages * vBytes;
     static constexpr uint32_t bytes = bars + 32 * 8;
 };
 
@@ -185,10 +176,9 @@ enum : int {
     kKEmpty = kKFull + kKStages,                       // [kKStages]
     kVFull = kKEmpty + kKStages,                       // [kVStages]
     kVEmpty = kVFull + kVStages,                       // [kVStages]
-    kSFull = kVEmpty + kVStages,                       // [kSBufs]
-    kPReady = kSFull + kSBufs,                         // [kSBufs]
-    kODone = kPReady + kSBufs,                         // [2], by PV parity
-    kOLast = kODone + 2,
+    kSFull = kVEmpty + kVStages,                       // [kQTiles]
+    kPReady = kSFull + kQTiles,                        // [kQTiles]
+    kOLast = kPReady + kQTiles,
     kTmemSlot = kOLast + 1,
     kAbortSlot = kTmemSlot + 1,
     kNumSlots = kAbortSlot + 1
@@ -197,8 +187,8 @@ static_assert(kNumSlots <= 32, "barrier area");
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    sage_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                          AttnArgs a)
+    sage_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, AttnArgs a)
 {
     using Lay = AttnLayout<D>;
     extern __shared__ uint8_t dyn_smem[];
@@ -209,27 +199,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::bars);
     uint64_t *q_full = bars + kQFull, *k_full = bars + kKFull, *k_empty = bars + kKEmpty;
     uint64_t *v_full = bars + kVFull, *v_empty = bars + kVEmpty, *s_full = bars + kSFull;
-    uint64_t *p_ready = bars + kPReady, *o_done = bars + kODone, *o_last = bars + kOLast;
+    uint64_t *p_ready = bars + kPReady, *o_last = bars + kOLast;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kTmemSlot);
     volatile int *abort = reinterpret_cast<volatile int *>(bars + kAbortSlot);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int t0 = blockIdx.x * kTile, j = blockIdx.y, b = blockIdx.z;
+    const int t0 = blockIdx.x * (kQTiles * kTile), j = blockIdx.y, b = blockIdx.z;
     const int bh = b * a.h + j;
     const int n = a.n, ntk = a.ntk;
 
     if (warp == kMmaWarp) tc::tmem_alloc(tmem_slot, kTmemCols);
-    // the constant rows of every V stage (TMA writes only the first D rows of
-    // each 64-key block): row D = 1.0, rows D+1 .. D+15 = 0
-    for (int x = tid; x < kVStages * 2 * 16 * 8; x += kAttnThreads) {
-        const int blk = x / 128, r = (x / 8) % 16, c = x % 8;
-        uint8_t *row = sm + Lay::v0 + (blk >> 1) * Lay::vBytes + (blk & 1) * (Lay::vRows * 128) + (D + r) * 128;
-        const uint32_t one2 = 0x3C003C00u;   // two fp16 ones
-        reinterpret_cast<uint4 *>(row)[c] = r == 0 ? make_uint4(one2, one2, one2, one2) : make_uint4(0, 0, 0, 0);
-    }
-    tc::fence_smem_to_async();
     if (tid == 0) {
-        tc::mbar_init(q_full, kSoftmaxThreads / 2);      // the half-0 softmax threads write Q
+        tc::mbar_init(q_full, 1);
         for (int s = 0; s < kKStages; ++s) {
             tc::mbar_init(k_full + s, 1);
             tc::mbar_init(k_empty + s, 1);
@@ -238,12 +219,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc::mbar_init(v_full + s, 1);
             tc::mbar_init(v_empty + s, 1);
         }
-        for (int s = 0; s < kSBufs; ++s) {
-            tc::mbar_init(s_full + s, 1);
-            tc::mbar_init(p_ready + s, kSoftmaxThreads);
+        for (int w = 0; w < kQTiles; ++w) {
+            tc::mbar_init(s_full + w, 1);
+            tc::mbar_init(p_ready + w, kSoftmaxThreads / kQTiles);
         }
-        tc::mbar_init(o_done, 1);
-        tc::mbar_init(o_done + 1, 1);
         tc::mbar_init(o_last, 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -252,27 +231,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    // O takes D + 16 columns, read in 32-column chunks: Q starts after them
-    const uint32_t tS0 = tmem, tO = tmem + kSBufs * kTile, tQ = tO + (D + 32);
+    // S_w at column 128 w, O_w at 256 + D w
+    const uint32_t tS0 = tmem, tO0 = tmem + kQTiles * kTile;
 
     if (warp == kKTmaWarp) {
-        // --------------------------------------------------------- TMA: K
+        // ------------------------------------------------------ TMA: Q, K
         if (lane == 0) {
+            // the two query tiles (rows past T read as zeros)
+            tc::mbar_expect_tx(q_full, kQTiles * Lay::tBytes);
+            for (int w = 0; w < kQTiles; ++w)
+                for (int kb = 0; kb < D / 64; ++kb)
+                    tc::tma_load_3d(sm + Lay::q0 + w * Lay::tBytes + kb * (kTile * 128), &tm_q, kb * 64,
+                                    t0 + w * kTile, bh, q_full);
             int last[kKStages];
             for (int s = 0; s < kKStages; ++s) last[s] = -1;
             for (int i = 0; i < ntk; ++i) {
                 const int s = i % kKStages;
-                // a K stage frees when its S product completes
+                // a K stage frees when both S products that read it complete
                 if (i >= kKStages &&
                     !tc::mbar_wait_abortable(k_empty + s, ((i / kKStages) - 1) & 1, kWaitNs, abort))
                     break;
-                tc::mbar_expect_tx(k_full + s, Lay::kBytes);
-                uint8_t *kd = sm + Lay::k0 + s * Lay::kBytes;
+                tc::mbar_expect_tx(k_full + s, Lay::tBytes);
+                uint8_t *kd = sm + Lay::k0 + s * Lay::tBytes;
                 for (int kb = 0; kb < D / 64; ++kb)
                     tc::tma_load_3d(kd + kb * (kTile * 128), &tm_k, kb * 64, i * kTile, bh, k_full + s);
                 last[s] = i;
             }
             if (*abort) {                      // let the copies in flight land
+                tc::mbar_wait(q_full, 0, kWaitNs);
                 for (int s = 0; s < kKStages; ++s)
                     if (last[s] >= 0) tc::mbar_wait(k_full + s, (last[s] / kKStages) & 1, kWaitNs);
             }
@@ -284,14 +270,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int s = 0; s < kVStages; ++s) last[s] = -1;
             for (int i = 0; i < ntk; ++i) {
                 const int s = i % kVStages;
-                // a V stage frees when its PV product completes
+                // a V stage frees when both PV products that read it complete
                 if (i >= kVStages &&
                     !tc::mbar_wait_abortable(v_empty + s, ((i / kVStages) - 1) & 1, kWaitNs, abort))
                     break;
-                tc::mbar_expect_tx(v_full + s, Lay::vLoadBytes);
+                tc::mbar_expect_tx(v_full + s, Lay::vBytes);
                 uint8_t *vd = sm + Lay::v0 + s * Lay::vBytes;
                 for (int c = 0; c < 2; ++c)
-                    tc::tma_load_3d(vd + c * (Lay::vRows * 128), &tm_v, i * kTile + c * 64, 0, bh, v_full + s);
+                    tc::tma_load_3d(vd + c * (D * 128), &tm_v, i * kTile + c * 64, 0, bh, v_full + s);
                 last[s] = i;
             }
             if (*abort) {
@@ -301,133 +287,122 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // -------------------------------------------------------- MMA issuer
-        // S_i = Q K_i^T runs a tile ahead of the softmax (two S buffers);
-        // S_{i+2} is issued after PV_i, which read P_i from that buffer (the
-        // tensor pipe runs in order).  Both products take their A operand
-        // (Q, P) from tensor memory and only B (K, V) from shared memory.
+        // Step i (0 <= i <= ntk): for w = A, B: O_w += P_w(i-1) V(i-1) once
+        // the warpgroup has written P_w(i-1), then S_w(i) = Q_w K_i^T.
         if (lane == 0) {
-            constexpr uint32_t idS = tc::idesc_f16_f32(kTile, kTile), idO = tc::idesc_f16_f32(kTile, Lay::vRows);
+            constexpr uint32_t idS = tc::idesc_f16_f32(kTile, kTile), idO = tc::idesc_f16_f32(kTile, D);
             bool ok = tc::mbar_wait_abortable(q_full, 0, kWaitNs, abort);
-            int nq = 0;                        // next S product to issue
-            for (int pv = 0; ok && pv < ntk; ++pv) {
-                for (; nq < ntk && nq <= pv + kSBufs - 1; ++nq) {
-                    const int ks = nq % kKStages, sb = nq % kSBufs;
-                    if (!(ok = tc::mbar_wait_abortable(k_full + ks, (nq / kKStages) & 1, kWaitNs, abort))) break;
-                    tc::fence_after_sync();
-                    const uint32_t ak = tc::smem_u32(sm + Lay::k0 + ks * Lay::kBytes);
+            const uint32_t aq = tc::smem_u32(sm + Lay::q0);
+            for (int i = 0; ok && i <= ntk; ++i) {
+                const int ks = i % kKStages, vs = (i + kVStages - 1) % kVStages;
+                uint32_t ak = 0, av = 0;
+                if (i < ntk) {
+                    if (!(ok = tc::mbar_wait_abortable(k_full + ks, (i / kKStages) & 1, kWaitNs, abort))) break;
+                    ak = tc::smem_u32(sm + Lay::k0 + ks * Lay::tBytes);
+                }
+                if (i >= 1) {
+                    if (!(ok = tc::mbar_wait_abortable(v_full + vs, ((i - 1) / kVStages) & 1, kWaitNs, abort)))
+                        break;
+                    av = tc::smem_u32(sm + Lay::v0 + vs * Lay::vBytes);
+                }
+                tc::fence_after_sync();
+                for (int w = 0; w < kQTiles; ++w) {
+                    const uint32_t tS = tS0 + w * kTile;
+                    if (i >= 1) {
+                        // A = P_w(i-1): fp16 pairs in the first 64 columns of S_w
+                        if (!(ok = tc::mbar_wait_abortable(p_ready + w, (i - 1) & 1, kWaitNs, abort))) break;
+                        tc::fence_after_sync();
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k)
-                        tc::mma_f16_ts(tS0 + sb * kTile, tQ + k * 8, tc::sw128_desc_k(ak, k, kTile), idS, k > 0);
-                    tc::mma_commit(s_full + sb);
-                    tc::mma_commit(k_empty + ks);
+                        for (int k = 0; k < kTile / 16; ++k)
+                            tc::mma_f16_ts(tO0 + w * D, tS + k * 8, tc::sw128_desc_k(av, k, D), idO,
+                                           (i > 1 || k > 0) ? 1u : 0u);
+                    }
+                    if (i < ntk) {
+                        const uint32_t aqw = aq + w * Lay::tBytes;
+#pragma unroll
+                        for (int k = 0; k < D / 16; ++k)
+                            tc::mma_f16(tS, tc::sw128_desc_k(aqw, k, kTile), tc::sw128_desc_k(ak, k, kTile), idS,
+                                        k > 0);
+                        tc::mma_commit(s_full + w);
+                    }
                 }
                 if (!ok) break;
-                // O += P_pv V_pv, A = P_pv: fp16 pairs in the first 64
-                // columns of its S buffer
-                const int sb = pv % kSBufs, vs = pv % kVStages;
-                if (!(ok = tc::mbar_wait_abortable(p_ready + sb, (pv / kSBufs) & 1, kWaitNs, abort))) break;
-                if (!(ok = tc::mbar_wait_abortable(v_full + vs, (pv / kVStages) & 1, kWaitNs, abort))) break;
-                tc::fence_after_sync();
-                const uint32_t av = tc::smem_u32(sm + Lay::v0 + vs * Lay::vBytes);
-#pragma unroll
-                for (int k = 0; k < kTile / 16; ++k)
-                    tc::mma_f16_ts(tO, tS0 + sb * kTile + k * 8, tc::sw128_desc_k(av, k, Lay::vRows), idO,
-                                   (pv > 0 || k > 0) ? 1u : 0u);
-                tc::mma_commit(o_done + (pv & 1));
-                tc::mma_commit(v_empty + vs);
-                if (pv == ntk - 1) tc::mma_commit(o_last);
+                if (i >= 1) tc::mma_commit(v_empty + vs);
+                if (i < ntk) tc::mma_commit(k_empty + ks);
             }
+            // completes when every product issued above has (also after an abort)
+            tc::mma_commit(o_last);
         }
     } else if (warp < 8) {
         // ---------------------------------------------------------- softmax
-        // warp w: TMEM lane quarter w % 4 (query rows), key half g = w / 4 of
-        // every tile (one 64-key group: one K scale per thread)
-        const int g = warp >> 2, row = (warp & 3) * 32 + lane;
-        const int t = t0 + row;
+        // warpgroup w = warp / 4 owns query tile w; warp % 4 picks the TMEM
+        // lane quarter, so the thread's row is its lane in S_w and O_w
+        const int w = warp >> 2, row = (warp & 3) * 32 + lane;
+        const int t = t0 + w * kTile + row;
         const float qa = t < n ? a.qs[(size_t)bh * a.wq + t / a.gq] * a.scale_log2 : 0.0f;
         const float *ksr = a.ks + (size_t)bh * a.wk;
-        float *red = reinterpret_cast<float *>(sm + Lay::red);   // [2][2 halves][128 rows]
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        constexpr int OC = (D + 32) / 32;      // 32-column chunks of O, the sum column included
-        constexpr int OC0 = (OC + 1) / 2;      // chunks [0, OC0) rescaled by half 0, the rest by half 1
-        // Q (widened, fp16) into tensor memory: row t -> lane, element pairs
-        // -> consecutive columns; half 0 of each row writes it
-        if (g == 0) {
-            const uint4 *qrow = reinterpret_cast<const uint4 *>(a.q16 + ((size_t)bh * a.T + t) * D);
-#pragma unroll
-            for (int cq = 0; cq < D / 64; ++cq) {
-                uint32_t r[32];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint4 w = qrow[cq * 8 + e];
-                    r[4 * e] = w.x;
-                    r[4 * e + 1] = w.y;
-                    r[4 * e + 2] = w.z;
-                    r[4 * e + 3] = w.w;
-                }
-                tc::tmem_st32u(tQ + lane_base + cq * 32, r);
-            }
-            tc::tmem_st_wait();
-            tc::fence_before_sync();
-            tc::mbar_arrive(q_full);
-        }
-        float m_use = -INFINITY;
-        bool ok = true, bad = false;
+        const uint32_t tS = tS0 + w * kTile + lane_base, tO = tO0 + w * D + lane_base;
+        float m_use = -INFINITY, l = 0.0f;
+        bool bad = false;
         // a warp-uniform outcome, so the warp-wide TMEM accesses stay converged
         auto wait_warp = [&](uint64_t *bar, uint32_t parity) {
             return __all_sync(0xffffffffu, tc::mbar_wait_abortable(bar, parity, kWaitNs, abort)) != 0;
         };
-        // A failed wait skips the work that needs it; the softmax warps leave
-        // the loop together, at the barrier where the halves meet.
         for (int i = 0; i < ntk; ++i) {
-            const int u0 = i * kTile, sb = i % kSBufs;
-            const int gk = u0 / 64 + g;                    // this thread's K group
-            const float c = gk < a.wk ? qa * ksr[gk] : 0.0f;
-            const int nvalid = min(max(n - u0 - g * 64, 0), 64);
-            if (!bad) bad = !wait_warp(s_full + sb, (i / kSBufs) & 1);
-            float x[64];
-            float mine = -INFINITY;
-            if (!bad) {
-                tc::fence_after_sync();
-                {
-                    uint32_t r0[32], r1[32];
-                    tc::tmem_ld32_issue(tS0 + sb * kTile + lane_base + g * 64, r0);
-                    tc::tmem_ld32_issue(tS0 + sb * kTile + lane_base + g * 64 + 32, r1);
-                    tc::tmem_ld_wait(r0);
-                    tc::tmem_pin(r1);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        x[e] = __uint_as_float(r0[e]);
-                        x[32 + e] = __uint_as_float(r1[e]);
-                    }
-                }
-                // x holds integer logits; c >= 0, so the half's max scaled
-                // logit is c * (max raw logit), and each weight is 2^fma(S, c, -m).
-                // Eight independent running maxima keep the chain short.
-                float m8[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
-                if (nvalid == 64) {
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) m8[e & 7] = fmaxf(m8[e & 7], x[e]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) m8[e & 7] = e < nvalid ? fmaxf(m8[e & 7], x[e]) : m8[e & 7];
-                }
-                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-                mine = nvalid > 0 ? c * mx : -INFINITY;
-            }
-            red[((i & 1) * 2 + g) * kTile + row] = mine;
-            // both halves of the row have read their S columns before either
-            // writes P over the first 64 of them
-            tc::fence_before_sync();
-            if (tc::bar_or(1, kSoftmaxThreads, bad || *abort)) {
-                ok = false;
+            const int u0 = i * kTile;
+            const int gk = u0 / 64;            // the tile's two K groups (their loads
+                                               // overlap the wait for S)
+            const float c0 = gk < a.wk ? qa * ksr[gk] : 0.0f;
+            const float c1 = gk + 1 < a.wk ? qa * ksr[gk + 1] : 0.0f;
+            const int nvalid = min(n - u0, kTile);
+            if (!wait_warp(s_full + w, i & 1)) {
+                bad = true;
                 break;
             }
             tc::fence_after_sync();
-            const float mt = fmaxf(mine, red[((i & 1) * 2 + (g ^ 1)) * kTile + row]);
+            // the row's 128 integer logits; c >= 0, so a half's max scaled
+            // logit is c times its max raw logit, and each weight is
+            // 2^fma(S, c, -m).  Eight independent running maxima per half keep
+            // the chains short.
+            float x[kTile];
+            {
+                uint32_t r0[32], r1[32], r2[32], r3[32];
+                tc::tmem_ld32_issue(tS, r0);
+                tc::tmem_ld32_issue(tS + 32, r1);
+                tc::tmem_ld32_issue(tS + 64, r2);
+                tc::tmem_ld32_issue(tS + 96, r3);
+                tc::tmem_ld_wait(r0);
+                tc::tmem_pin(r1);
+                tc::tmem_pin(r2);
+                tc::tmem_pin(r3);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    x[e] = __uint_as_float(r0[e]);
+                    x[32 + e] = __uint_as_float(r1[e]);
+                    x[64 + e] = __uint_as_float(r2[e]);
+                    x[96 + e] = __uint_as_float(r3[e]);
+                }
+            }
+            float mh[2];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float m8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+                if (nvalid == kTile) {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) m8[e & 7] = fmaxf(m8[e & 7], x[hf * 64 + e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e)
+                        m8[e & 7] = hf * 64 + e < nvalid ? fmaxf(m8[e & 7], x[hf * 64 + e]) : m8[e & 7];
+                }
+                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                mh[hf] = hf * 64 < nvalid ? (hf == 0 ? c0 : c1) * mx : -INFINITY;
+            }
+            const float mt = fmaxf(mh[0], mh[1]);
             const bool grow = mt > m_use + kRescaleLog2;   // always on the first tile
             float alpha = 1.0f;
             if (grow) {
@@ -435,73 +410,70 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 m_use = mt;
             }
             const float nm = -m_use;
-            uint32_t pk[32];
-            if (nvalid == 64) {
-                // exponents two at a time (packed fma.rn.f32x2: the same
-                // rounding as two fmaf); three passes over the 64 values
-                // (exponents, exp2, fp16 pairs) keep 64 independent
-                // operations in flight per step
-                const uint64_t c2 = f2pack(c, c), nm2 = f2pack(nm, nm);
+            float ls;
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    f2unpack(f2fma(f2pack(x[2 * e], x[2 * e + 1]), c2, nm2), x[2 * e], x[2 * e + 1]);
+            for (int hf = 0; hf < 2; ++hf) {
+                const float c = hf == 0 ? c0 : c1;
+                float *xh = x + hf * 64;
+                uint32_t pk[32];
+                if (nvalid == kTile) {
+                    // exponents two at a time (packed fma.rn.f32x2: the same
+                    // rounding as two fmaf), then exp2
+                    const uint64_t c2 = f2pack(c, c), nm2 = f2pack(nm, nm);
 #pragma unroll
-                for (int e = 0; e < 64; ++e) x[e] = ex2(x[e]);
+                    for (int e = 0; e < 32; ++e)
+                        f2unpack(f2fma(f2pack(xh[2 * e], xh[2 * e + 1]), c2, nm2), xh[2 * e], xh[2 * e + 1]);
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) xh[e] = ex2(xh[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) xh[e] = hf * 64 + e < nvalid ? ex2(fmaf(xh[e], c, nm)) : 0.0f;
+                }
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const __half2 hp = __floats2half2_rn(x[2 * e], x[2 * e + 1]);
+                    const __half2 hp = __floats2half2_rn(xh[2 * e], xh[2 * e + 1]);
                     pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
-            } else {
+                // P of this half's 64 keys over S_w columns 32 hf .. 32 hf + 31;
+                // the half's weight sum (four packed partial sums) overlaps the store
+                tc::tmem_st32u(tS + hf * 32, pk);
+                uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float p0 = 2 * e < nvalid ? ex2(fmaf(x[2 * e], c, nm)) : 0.0f;
-                    const float p1 = 2 * e + 1 < nvalid ? ex2(fmaf(x[2 * e + 1], c, nm)) : 0.0f;
-                    const __half2 hp = __floats2half2_rn(p0, p1);
-                    pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
-                }
+                for (int e = 0; e < 32; ++e) acc[e & 3] = f2add(acc[e & 3], f2pack(xh[2 * e], xh[2 * e + 1]));
+                float s0, s1, s2, s3, s4, s5, s6, s7;
+                f2unpack(acc[0], s0, s1);
+                f2unpack(acc[1], s2, s3);
+                f2unpack(acc[2], s4, s5);
+                f2unpack(acc[3], s6, s7);
+                const float hs = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+                ls = hf == 0 ? hs : ls + hs;
             }
-            // P over the first 64 columns of this tile's S buffer (half g
-            // writes columns 32 g .. 32 g + 31)
-            tc::tmem_st32u(tS0 + sb * kTile + lane_base + g * 32, pk);
-            tc::tmem_st_wait();
-            // O *= alpha where the max grew: O must first hold PV_{i-1}.
-            // PV products alternate between two barriers; S_i was issued
-            // after PV_{i-2} and has completed, so barrier (i-1) & 1 has
-            // completed either the phase waited for or the one before it, and
-            // the parity cannot alias.
+            l = l * alpha + ls;
+            // O_w *= alpha where the max grew: S_w(i) completing means PV_w(i-1),
+            // issued before it, has completed too
             if (i >= 1 && __any_sync(0xffffffffu, grow)) {
-                bad = !wait_warp(o_done + ((i - 1) & 1), ((i - 1) >> 1) & 1);
-                if (bad) continue;             // the next barrier takes everyone out
-                tc::fence_after_sync();
 #pragma unroll
-                for (int cc = 0; cc < OC; ++cc) {
-                    if ((cc < OC0) != (g == 0)) continue;
+                for (int cc = 0; cc < D / 32; ++cc) {
                     float v[32];
-                    tc::tmem_ld32(tO + lane_base + cc * 32, v);
+                    tc::tmem_ld32(tO + cc * 32, v);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] *= alpha;
-                    tc::tmem_st32(tO + lane_base + cc * 32, v);
+                    tc::tmem_st32(tO + cc * 32, v);
                 }
-                tc::tmem_st_wait();
             }
+            tc::tmem_st_wait();
             tc::fence_before_sync();
-            tc::mbar_arrive(p_ready + sb);
+            tc::mbar_arrive(p_ready + w);
         }
-        if (ok && !bad && wait_warp(o_last, 0)) {
+        if (!bad && wait_warp(o_last, 0)) {
             tc::fence_after_sync();
-            float inv_l;
-            {
-                float v[32];
-                tc::tmem_ld32(tO + lane_base + D, v);      // column D: the sum of the weights
-                inv_l = 1.0f / v[0];
-            }
+            const float inv_l = 1.0f / l;
             const float *vsc = a.vs + (size_t)bh * D;
             const size_t orow = (((size_t)b * n + t) * a.h + j) * D;
 #pragma unroll
-            for (int cc = g * (D / 64); cc < (g + 1) * (D / 64); ++cc) {
+            for (int cc = 0; cc < D / 32; ++cc) {
                 float v[32];
-                tc::tmem_ld32(tO + lane_base + cc * 32, v);
+                tc::tmem_ld32(tO + cc * 32, v);
                 if (t < n) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = v[e] * inv_l * vsc[cc * 32 + e];
@@ -510,29 +482,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                         for (int e = 0; e < 8; ++e) o[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
                     } else {
-                        uint32_t w[16];
+                        uint32_t ww[16];
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             if (a.out_dtype == ULP_BF16) {
                                 const __nv_bfloat162 hv = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-                                w[e] = *reinterpret_cast<const uint32_t *>(&hv);
+                                ww[e] = *reinterpret_cast<const uint32_t *>(&hv);
                             } else {
                                 const __half2 hv = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
-                                w[e] = *reinterpret_cast<const uint32_t *>(&hv);
+                                ww[e] = *reinterpret_cast<const uint32_t *>(&hv);
                             }
                         }
                         uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.out) + orow + cc * 32);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) o[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                        for (int e = 0; e < 4; ++e) o[e] = make_uint4(ww[4 * e], ww[4 * e + 1], ww[4 * e + 2], ww[4 * e + 3]);
                     }
                 }
             }
         }
     }
 
-    // every role is done (or gave up); the CTA's tensor-core work has
-    // completed unless a wait timed out, in which case the last products get
-    // one more bounded wait before the tensor memory is released
+    // every role is done (or gave up); the MMA thread's last commit covers
+    // every product it issued, so after an abort one more bounded wait on it
+    // comes before the tensor memory is released
     tc::fence_before_sync();
     __syncthreads();
     if (*abort) {
@@ -632,7 +604,8 @@ extern "C" int ulp_sage_attention(const int8_t *q8, const int8_t *k8, const uint
     const size_t plane = (size_t)B * h * T * D;
     uint16_t *q16 = reinterpret_cast<uint16_t *>(workspace), *k16 = q16 + plane, *v16 = k16 + plane;
 
-    CUtensorMap mk, mv;
+    CUtensorMap mq, mk, mv;
+    if (int s = make_map(&mq, q16, D, T, (uint64_t)B * h, kTile)) return s;
     if (int s = make_map(&mk, k16, D, T, (uint64_t)B * h, kTile)) return s;
     if (int s = make_map(&mv, v16, T, D, (uint64_t)B * h, D)) return s;
 
@@ -650,20 +623,19 @@ extern "C" int ulp_sage_attention(const int8_t *q8, const int8_t *k8, const uint
     a.wq = (n + q_group - 1) / q_group;
     a.wk = (n + kGK - 1) / kGK;
     a.ntk = T / kTile;
-    a.T = T;
-    a.q16 = q16;
     a.scale_log2 = sm_scale * 1.4426950408889634f;
-    const dim3 grid((unsigned)a.ntk, (unsigned)h, (unsigned)B);
+    // a CTA per pair of query tiles; an odd last tile's partner reads zeros
+    const dim3 grid((unsigned)((a.ntk + kQTiles - 1) / kQTiles), (unsigned)h, (unsigned)B);
     // one CTA per SM (it holds all 512 TMEM columns): at D = 64 the request
     // is padded past half of the SM's shared memory
     if (D == 128) {
         const size_t bytes = AttnLayout<128>::bytes + 1024;
         cudaFuncSetAttribute(sage_attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-        sage_attention_kernel<128><<<grid, kAttnThreads, bytes, st>>>(mk, mv, a);
+        sage_attention_kernel<128><<<grid, kAttnThreads, bytes, st>>>(mq, mk, mv, a);
     } else {
         const size_t bytes = std::max<size_t>(AttnLayout<64>::bytes + 1024, 120 * 1024);
         cudaFuncSetAttribute(sage_attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-        sage_attention_kernel<64><<<grid, kAttnThreads, bytes, st>>>(mk, mv, a);
+        sage_attention_kernel<64><<<grid, kAttnThreads, bytes, st>>>(mq, mk, mv, a);
     }
     return check_launch("sage_attention");
 }

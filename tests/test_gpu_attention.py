@@ -11,15 +11,17 @@ Vmax = max over the live keys of |V[u, d]| for that batch, head and channel):
     itself shifts every weight alike and cancels.  So each weight 2^(x - m)
     is off by at most ln2 * 6 * 2^-24 * xmax relative, plus the 2^-22 of the
     hardware exp2;
-  * each weight is rounded to fp16 (2^-11 relative in the normal range,
-    2^-25 absolute below it) and the denominator sums the rounded weights, so
-    the output is a weighted mean with weights perturbed by
-    eps_w = 2^-11 + 6 ln2 2^-24 xmax + 2^-22 relative: error <= 2 eps_w Vmax,
-    plus n 2^-25 Vmax for the subnormal weights;
-  * fp32 accumulation of the n products in the PV MMAs and the O rescales,
-    for the numerator and (through a row of ones in V) the denominator alike:
-    <= 2 (n + ntiles) 2^-23 Vmax; the final scaling by 1/l and v_scale:
-    3 2^-24.
+  * so the computed weights' mean is within 2 eps_e Vmax of the exact one,
+    eps_e = 6 ln2 2^-24 xmax + 2^-22;
+  * the numerator's weights are rounded to fp16 (2^-11 relative in the
+    normal range, 2^-25 absolute below it) while the denominator sums the
+    fp32 weights: at most 2^-11 Vmax more, plus n 2^-25 Vmax for the
+    subnormal weights (the largest weight of a row is >= 1, so the sum is);
+    with eps_w = 2^-11 + eps_e, 2 eps_e + 2^-11 <= 2 eps_w;
+  * fp32 accumulation of the n products in the PV MMAs and the O rescales
+    (numerator), and of the row's weights in eight partial sums per tile and
+    one running sum across tiles (denominator): <= 2 (n + ntiles) 2^-23
+    Vmax together; the final scaling by 1/l and v_scale: 3 2^-24.
 bound(n, xmax) = 2 eps_w + n (2^-22 + 2^-25) + (2 ceil(n/128) + 3) 2^-23.
 bf16 / fp16 outputs add one rounding of the result (2^-9 / 2^-12 relative).
 """
