@@ -277,17 +277,18 @@ int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int D, int wor
 
 /* Attention over the unpacked tensors of one destination -- the consumer the
  * page "unpack_for_sage" hands its outputs to (INT8 Q/K, FP8 E4M3 V, FP32
- * scales of width scale_widths(n) derived from the n rows attended over; "V
- * scale remains with the caller and must be passed separately to
- * attention").  The pages print no formula for it; this library's reading,
+ * scales of width scale_widths(n) derived from the n rows attended over; the
+ * V scale is not in the chunks, so the caller supplies it here, per that
+ * page's Returns section).  The pages print no formula for it; this library's reading,
  * non-causal softmax attention over the live prefix t, u < n:
  *   Q[t] = q8[t] * q_scale[t / q_group], K[u] = k8[u] * k_scale[u / 64],
  *   V[u, d] = e4m3(v8[d, u]) * v_scale[d],
  *   O[b, t, j, :] = sum_u softmax_u(sm_scale * Q[t] . K[u]) V[u]
  * (K centred by the mean attends the same: q . m is one constant per query).
  * Computed on tensor cores with fp16 operands and fp32 accumulation: the
- * integer logits are exact, P is rounded to fp16 (relative 2^-11) and the
- * denominator sums the rounded values.  A first kernel widens Q, K and V to
+ * integer logits are exact, P is rounded to fp16 (relative 2^-11) for the PV
+ * product and the denominator sums the fp32 weights, so rounding P moves the
+ * output by at most 2^-11 of max |V|.  A first kernel widens Q, K and V to
  * fp16 in the workspace (at least ulp_sage_attention_workspace_bytes bytes;
  * contents on return unspecified), the second runs the attention from it.
  *   q8, k8    [B, S, h, D] int8 (rows >= n are not read)

@@ -313,8 +313,9 @@ void orc_k_grouped_amax(const uint16_t *k, const uint16_t *k_mean, int dtype, in
 /* ------------------------------------------------ boundary min/max producer */
 
 /* Raw-K boundary min/max of rank r, the payload of "AllGather #1" (page
- * "derive_k_boundary_amax": gathered_minmax is [P, B, H, 2, 2, D] raw-K
- * boundary min/max; a padding-only slice carries min=+inf, max=-inf).
+ * "derive_k_boundary_amax", Parameters: the gathered buffer has shape
+ * [P, B, H, 2, 2, D]; a slice with only padding rows contributes min=+inf,
+ * max=-inf).
  * Readings: axis 3 is e (0 = first touched K group, 1 = last), axis 4 is the
  * statistic (0 = min, 1 = max); only live rows t < used count; a rank that
  * touches one group writes it under both e; -0 is stored as +0.

@@ -264,8 +264,9 @@ def boundary_minmax(k: torch.Tensor, q: torch.Tensor, *, rank: Optional[int], wo
 def derive_k_boundary_amax(grouped_amax: torch.Tensor, gathered_minmax: torch.Tensor,
                            k_mean_global: torch.Tensor, *, rank: Optional[int],
                            local_sequence: int, world_size: int) -> torch.Tensor:
-    """Overwrite the rank's K boundary slots with the derived cross-rank amax,
-    in place (page "derive_k_boundary_amax")."""
+    """In place: the rank's first and last K group slots take the amax
+    rebuilt from every touching rank's raw-K min/max (page
+    "derive_k_boundary_amax")."""
     B, H, D = k_mean_global.shape
     _check(lib().ulp_derive_k_boundary_amax(_ptr(grouped_amax), _ptr(gathered_minmax),
                                             _ptr(k_mean_global), _dtype_code(k_mean_global), B, H,
