@@ -312,6 +312,20 @@ int ulp_sage_attention(const int8_t *q8, const int8_t *k8, const uint8_t *v8, co
  * (Q, K, V in fp16 over the live prefix rounded up to 128 rows). */
 int ulp_sage_attention_workspace_bytes(int B, int S, int h, int D, int n, size_t *bytes);
 
+/* Debug check of a precondition of the path (page
+ * "flashinfer.comm._ulysses_lowp.k_grouped_amax", Parameters: used_sequence):
+ * the input rows past the live count are zero.  Counts the elements of Q, K
+ * and V in global rows t >= used_sequence whose value is not +0 or -0, over
+ * the shard of `rank` (or, for ULP_ALL_RANKS, over all P stacked shards), and
+ * adds the count to *count, a device uint64 the caller zeroes.  Nothing is
+ * launched when used_sequence is -1 or S.  -0 counts as zero: it moves no
+ * amax and no code.
+ *   q, k, v  [B, L, H, D] dtype ([P, B, L, H, D] for ULP_ALL_RANKS), 16-byte aligned
+ *   count    device uint64, 8-byte aligned */
+int ulp_check_padding(const void *q, const void *k, const void *v, int dtype, int B, int L, int H, int D,
+                      int rank, int world_size, int used_sequence, unsigned long long *count,
+                      ulp_stream_t stream);
+
 /* Message of the calling thread's last failed call ("" if none). */
 const char *ulp_last_error(void);
 

@@ -241,6 +241,47 @@ static int grid_of(long long blocks, unsigned *out, const char *what)
     return ULP_OK;
 }
 
+
+// ------------------------------------------------- padding-row debug check
+
+struct PadArgs {
+    const uint16_t *t[3];          // q, k, v
+    unsigned long long *count;
+    int B, L, HD, rank, used;
+};
+
+// Elements of a 32-bit word (two 16-bit floats) whose value is not +-0.
+__device__ __forceinline__ unsigned nonzero2(uint32_t w)
+{
+    return ((w & 0x7FFFu) != 0u) + ((w & 0x7FFF0000u) != 0u);
+}
+
+// blockIdx.y = shard slot * B + batch; threads stride over the 16-byte
+// vectors of the shard's rows at or past `used` in the three tensors.
+__global__ void __launch_bounds__(256) check_padding_kernel(PadArgs a)
+{
+    const int z = blockIdx.y;
+    const int rk = z / a.B, b = z - rk * a.B;
+    const int r = a.rank >= 0 ? a.rank : rk;
+    const int first = max(0, a.used - r * a.L);        // the shard's first padding row
+    if (first >= a.L) return;                          // whole CTA: none here
+    const int nv = a.HD / 8;                           // vectors per row
+    const long long total = (long long)(a.L - first) * nv;
+    unsigned cnt = 0;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long row = first + i / nv;
+        const size_t off = (((size_t)rk * a.B + b) * a.L + (size_t)row) * a.HD + (size_t)(i % nv) * 8;
+#pragma unroll
+        for (int x = 0; x < 3; ++x) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(a.t[x] + off);
+            cnt += nonzero2(w.x) + nonzero2(w.y) + nonzero2(w.z) + nonzero2(w.w);
+        }
+    }
+    cnt = __reduce_add_sync(0xffffffffu, cnt);
+    if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(a.count, (unsigned long long)cnt);
+}
+
 }  // namespace ulp
 
 using namespace ulp;
@@ -296,6 +337,25 @@ int ulp_derive_k_boundary_amax(float *grouped_amax, const float *gathered_minmax
     if (int s = grid_of((long long)nranks * B * H * 2, &grid, "derive_k_boundary_amax")) return s;
     ULP_DISPATCH(D, dtype, (launch_kernel(derive_kernel<kD, kDT>, dim3(grid), dim3(kD), (cudaStream_t)stream, false, a)));
     return check_launch("derive_k_boundary_amax");
+}
+
+int ulp_check_padding(const void *q, const void *k, const void *v, int dtype, int B, int L, int H, int D,
+                      int rank, int world_size, int used_sequence, unsigned long long *count,
+                      ulp_stream_t stream)
+{
+    if (int s = check_common(dtype, B, L, H, D, rank, world_size, used_sequence, -1)) return s;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || ((uintptr_t)count & 7u) != 0)
+        return fail(ULP_EALIGN, "check_padding: q, k, v must be 16-byte aligned, count 8-byte aligned");
+    const int used = used_sequence < 0 ? L * world_size : used_sequence;
+    if (used == L * world_size) return ULP_OK;        // no padding rows
+    const int nranks = rank == ULP_ALL_RANKS ? world_size : 1;
+    if ((long long)nranks * B > 65535) return fail(ULP_EINVAL, "check_padding: ranks x batch above 65535");
+    PadArgs a{{(const uint16_t *)q, (const uint16_t *)k, (const uint16_t *)v}, count, B, L, H * D,
+              rank, used};
+    const long long vecs = (long long)L * H * D / 8;  // at most one shard's rows
+    const unsigned gx = (unsigned)std::min<long long>((vecs + 255) / 256, 4096);
+    check_padding_kernel<<<dim3(gx, (unsigned)(nranks * B)), 256, 0, (cudaStream_t)stream>>>(a);
+    return check_launch("check_padding");
 }
 
 }  // extern "C"

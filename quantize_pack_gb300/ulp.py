@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
         L.ulp_k_grouped_amax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P]
         L.ulp_boundary_minmax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]
         L.ulp_derive_k_boundary_amax.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]
+        L.ulp_check_padding.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P]
         L.ulp_pack.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                                _P, _I, _I, _P]
         L.ulp_alltoall_emulate.argtypes = [_P, _P, _I, _SZ, _P]
@@ -76,6 +77,7 @@ def lib() -> ctypes.CDLL:
                      "ulp_k_mean_workspace_bytes", "ulp_k_mean_global", "ulp_k_mean_global_noalloc",
                      "ulp_k_mean_global_grouped",
                      "ulp_k_grouped_amax", "ulp_boundary_minmax", "ulp_derive_k_boundary_amax",
+                     "ulp_check_padding",
                      "ulp_pack", "ulp_alltoall_emulate", "ulp_unpack_for_sage",
                      "ulp_sage_attention", "ulp_sage_attention_workspace_bytes"):
             getattr(L, name).restype = _I
@@ -240,6 +242,19 @@ def k_grouped_amax(k: torch.Tensor, k_mean_global: torch.Tensor, *, rank: Option
                                     world_size, _opt(used_sequence), _ptr(out), _pdl(enable_pdl),
                                     _stream(k.device)))
     return out
+
+
+def check_padding(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, rank: Optional[int],
+                  world_size: int, used_sequence: Optional[int] = None) -> int:
+    """Debug check of the precondition that input rows past used_sequence are
+    zero (page "k_grouped_amax", used_sequence parameter): the number of Q, K
+    and V elements in those rows that are not +-0 (0 when the inputs obey it).
+    Waits for the count on the current stream."""
+    rc, nr, B, L, H, D = _rank_dims(q, rank)
+    count = torch.zeros(1, dtype=torch.int64, device=q.device)
+    _check(lib().ulp_check_padding(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, L, H, D, rc, world_size,
+                                   _opt(used_sequence), _ptr(count), _stream(q.device)))
+    return int(count.item())
 
 
 def boundary_minmax(k: torch.Tensor, q: torch.Tensor, *, rank: Optional[int], world_size: int,

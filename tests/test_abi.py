@@ -77,6 +77,28 @@ def test_k_grouped_amax_rejects(lib, args, status):
     assert lib.ulp_last_error() != b""
 
 
+@pytest.mark.parametrize("args,status", [
+    (dict(dtype=7), -2), (dict(world_size=3), -1), (dict(rank=2, world_size=2), -1),
+    (dict(used=0), -1), (dict(used=2 * 96 + 1), -1),
+    (dict(q=FAKE + 8), -3), (dict(v=FAKE + 4), -3), (dict(count=FAKE + 4), -3),
+])
+def test_check_padding_rejects(lib, args, status):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, dtype=0, B=1, L=96, H=8, D=64, rank=-1, world_size=2, used=150,
+             count=FAKE)
+    a.update(args)
+    got = lib.ulp_check_padding(a["q"], a["k"], a["v"], a["dtype"], a["B"], a["L"], a["H"], a["D"],
+                                a["rank"], a["world_size"], a["used"], a["count"], None)
+    assert got == status
+    assert lib.ulp_last_error() != b""
+
+
+def test_check_padding_without_padding_launches_nothing(lib):
+    # used = -1 or S: no row to check, so the call returns before touching
+    # the (fake) device pointers
+    for used in (-1, 2 * 96):
+        assert lib.ulp_check_padding(FAKE, FAKE, FAKE, 0, 1, 96, 8, 64, -1, 2, used, FAKE, None) == 0
+
+
 def test_unpack_rejects(lib):
     ok = dict(recv=FAKE, B=1, L=96, h=4, D=64, P=2, aligned=-1, sseq=-1, gq=128, q8=FAKE,
               k8=FAKE, v8=FAKE, qs=FAKE, ks=FAKE, nd=1, pdl=-1)
