@@ -362,6 +362,19 @@ def run_ours(args, wl, rank, world, dist):
     torch.cuda.synchronize()
     kmean_ms = ks0.elapsed_time(ks1) / KM
 
+    # ---- the standalone k_grouped_amax of every rank (the public call and
+    # the unfused mode; the fused step computes it inside pack): reads K once
+    amax_out = torch.empty((wl.P, wl.B, wl.H, ulp.slots(wl.L, 64)), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        ulp.k_grouped_amax(k, km, rank=None, world_size=wl.P, used_sequence=wl.used_sequence, out=amax_out)
+    kg0, kg1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kg0.record(stream)
+    for _ in range(KM):
+        ulp.k_grouped_amax(k, km, rank=None, world_size=wl.P, used_sequence=wl.used_sequence, out=amax_out)
+    kg1.record(stream)
+    torch.cuda.synchronize()
+    kgamax_ms = kg0.elapsed_time(kg1) / KM
+
     # ---- the step after the path: attention over destination 0's outputs
     n_att = wl.used_sequence or wl.S
     q8, k8, v8, qsc, ksc = (o[0] for o in path.out)
@@ -461,6 +474,11 @@ def run_ours(args, wl, rank, world, dist):
                           "achieved_gbs": 2 * wl.N / (kmean_ms * 1e-3) / 1e9,
                           "frac": 2 * wl.N / (kmean_ms * 1e-3) / 1e9 / peak,
                           "note": "the step before the path (reads K once); not in value"},
+        "k_grouped_amax": {"ms": kgamax_ms, "calls": KM,
+                           "achieved_gbs": 2 * wl.N / (kgamax_ms * 1e-3) / 1e9,
+                           "frac": 2 * wl.N / (kgamax_ms * 1e-3) / 1e9 / peak,
+                           "note": "the standalone call over all ranks (2N bytes: K read once); "
+                                   "the fused step does this inside pack; not in value"},
         "attention": {"ms": att_ms, "calls": KA, "tflops": att_flops / (att_ms * 1e-3) / 1e12,
                       "peak": tensor_peak()[0], "peak_kind": tensor_peak()[1],
                       "frac": att_flops / (att_ms * 1e-3) / 1e12 / tensor_peak()[0],
