@@ -29,13 +29,17 @@ struct PackArgs {
     int early;   // read q, k, v, k_mean, v_scale before waiting for the preceding kernel
 };
 
-constexpr int kPackThreads = 512;
+// Threads per CTA: every thread holds 4 rows of 16-byte vectors per tensor at
+// either head size (512 at D = 128, 256 at D = 64), and 1024 threads stay
+// resident per SM at 64 registers.
+template <int D>
+constexpr int pack_threads() { return 4 * D; }
 constexpr int kSlab = 128;   // rows of a slab: one 128-row group = two 64-row groups
 
 template <int D>
 struct PackSmem {
     uint4 vtile[kSlab * D / 8];               // V rows of the slab
-    float red[kPackThreads / 32][4];          // per-warp Q0, Q1, K0, K1 maxima
+    float red[pack_threads<D>() / 32][4];     // per-warp Q0, Q1, K0, K1 maxima
     Int8Scale scl[4];                         // Q (first half), Q second half, K group 0, K group 1
     float vs[D], vr[D];                       // V channel scales and their reciprocals
 };
@@ -51,9 +55,9 @@ template <int D, int DT, int GQ, bool FULL>
 __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, PackSmem<D> &sm)
 {
     constexpr int NV = D / 8;                 // 16-byte vectors per row
-    constexpr int RL = kPackThreads / NV;     // row lanes
+    constexpr int RL = pack_threads<D>() / NV; // row lanes
     constexpr int IT = kSlab / RL;            // rows per thread
-    constexpr int NW = kPackThreads / 32;
+    constexpr int NW = pack_threads<D>() / 32;
     constexpr int NQH = kSlab / GQ;           // Q groups per slab
     static_assert(IT % 2 == 0 && RL * IT / 2 == kGK, "slab halves must be the K groups");
     static_assert(GQ == 64 || GQ == 128, "Q groups of 64 or 128 rows");
@@ -324,7 +328,7 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
 //     the scales;
 //  4. Q/K codes from the registers; 5. V codes from shared memory.
 template <int D, int DT, int GQ>
-__global__ void __launch_bounds__(kPackThreads, 2) pack_kernel(PackArgs a)
+__global__ void __launch_bounds__(pack_threads<D>(), 1024 / pack_threads<D>()) pack_kernel(PackArgs a)
 {
     __shared__ __align__(16) PackSmem<D> sm;
     pdl_trigger();
@@ -393,11 +397,11 @@ extern "C" int ulp_pack(const void *q, const void *k, const void *v, const void 
 #define ULP_PACK_LAUNCH(GQ_)                                                                         \
     do {                                                                                             \
         if (D == 128) {                                                                              \
-            if (dtype == ULP_BF16) launch_kernel(pack_kernel<128, ULP_BF16, GQ_>, grid, dim3(kPackThreads), st, pdl, a); \
-            else launch_kernel(pack_kernel<128, ULP_FP16, GQ_>, grid, dim3(kPackThreads), st, pdl, a);                   \
+            if (dtype == ULP_BF16) launch_kernel(pack_kernel<128, ULP_BF16, GQ_>, grid, dim3(pack_threads<128>()), st, pdl, a); \
+            else launch_kernel(pack_kernel<128, ULP_FP16, GQ_>, grid, dim3(pack_threads<128>()), st, pdl, a);                   \
         } else {                                                                                     \
-            if (dtype == ULP_BF16) launch_kernel(pack_kernel<64, ULP_BF16, GQ_>, grid, dim3(kPackThreads), st, pdl, a);  \
-            else launch_kernel(pack_kernel<64, ULP_FP16, GQ_>, grid, dim3(kPackThreads), st, pdl, a);                    \
+            if (dtype == ULP_BF16) launch_kernel(pack_kernel<64, ULP_BF16, GQ_>, grid, dim3(pack_threads<64>()), st, pdl, a);  \
+            else launch_kernel(pack_kernel<64, ULP_FP16, GQ_>, grid, dim3(pack_threads<64>()), st, pdl, a);                    \
         }                                                                                            \
     } while (0)
     if (q_group == 128) ULP_PACK_LAUNCH(128);
