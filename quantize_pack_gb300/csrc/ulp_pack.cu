@@ -29,43 +29,55 @@ struct PackArgs {
     int early;   // read q, k, v, k_mean, v_scale before waiting for the preceding kernel
 };
 
-// Threads per CTA: every thread holds 4 rows of 16-byte vectors per tensor at
-// either head size (512 at D = 128, 256 at D = 64), and 1024 threads stay
-// resident per SM at 64 registers.
-template <int D>
-constexpr int pack_threads() { return 4 * D; }
 constexpr int kSlab = 128;   // rows of a slab: one 128-row group = two 64-row groups
 
-template <int D>
+// Rows per CTA: a whole slab, or at D = 128 with 64-row Q groups one 64-row
+// half (one K group, one Q group), so that four CTAs stay resident per SM.
+// A 128-row Q group stays in one CTA: splitting it across two cost more than
+// it saved (a cluster exchange of the two maxima, or each half also reading
+// the other's Q rows).  Every thread holds 4 rows of 16-byte vectors per
+// tensor, so a CTA has R * D / 32 threads (512 or 256).
+template <int D, int GQ>
+constexpr int pack_rows() { return D == 128 && GQ == 64 ? 64 : 128; }
+template <int D, int GQ>
+constexpr int pack_threads() { return pack_rows<D, GQ>() * D / 32; }
+
+template <int D, int GQ>
 struct PackSmem {
-    uint4 vtile[kSlab * D / 8];               // V rows of the slab
-    float red[pack_threads<D>() / 32][4];     // per-warp Q0, Q1, K0, K1 maxima
-    Int8Scale scl[4];                         // Q (first half), Q second half, K group 0, K group 1
-    float vs[D], vr[D];                       // V channel scales and their reciprocals
+    uint4 vtile[pack_rows<D, GQ>() * D / 8];      // V rows of the CTA
+    float red[pack_threads<D, GQ>() / 32][4];     // per-warp Q0, Q1, K0, K1 maxima
+    Int8Scale scl[4];                             // Q (first / second group), K (first / second group)
+    float vs[D], vr[D];                           // V channel scales and their reciprocals
 };
 
 struct Slab {
     int rk, r, b, hh, js, g, L, S, row0, ts, fk, lk, tk, gu;   // js, ts: slab slot, touched slabs
 };
 
-// One slab: FULL = all 128 rows belong to the rank and none is excluded from
-// the K amax (so no per-row predicate is needed).  GQ = Q group rows: 128 (one
-// Q group per slab, slot js) or 64 (Q groups are the K groups 2g, 2g+1).
+// The CTA's rows of one slab: R = pack_rows<D, GQ>() rows from
+// tb = 128 g + R hs.  FULL = all of them belong to the rank and none is
+// excluded from the K amax (so no per-row predicate is needed).  GQ = Q group
+// rows: 128 (the slab's group, slot js) or 64 (the K groups).
 template <int D, int DT, int GQ, bool FULL>
-__device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, PackSmem<D> &sm)
+__device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, int half, PackSmem<D, GQ> &sm)
 {
+    constexpr int R = pack_rows<D, GQ>();     // rows of the CTA
     constexpr int NV = D / 8;                 // 16-byte vectors per row
-    constexpr int RL = pack_threads<D>() / NV; // row lanes
-    constexpr int IT = kSlab / RL;            // rows per thread
-    constexpr int NW = pack_threads<D>() / 32;
-    constexpr int NQH = kSlab / GQ;           // Q groups per slab
-    static_assert(IT % 2 == 0 && RL * IT / 2 == kGK, "slab halves must be the K groups");
+    constexpr int RL = pack_threads<D, GQ>() / NV;   // row lanes
+    constexpr int IT = R / RL;                // rows per thread
+    constexpr int NW = pack_threads<D, GQ>() / 32;
+    constexpr int KG = R / kGK;               // K groups of the CTA
+    constexpr int NQH = R / GQ;               // Q groups of the CTA
+    static_assert(IT == 4, "4 rows per thread");
+    static_assert(IT % KG == 0 && RL * IT / KG == kGK, "the CTA's rows split into whole K groups");
     static_assert(GQ == 64 || GQ == 128, "Q groups of 64 or 128 rows");
 
     const int c = threadIdx.x % NV, rl = threadIdx.x / NV;
     const int L = sl.L, row0 = sl.row0, g = sl.g;
     const size_t HD = (size_t)a.H * D;
-    const int t_first = g * kSlab + rl;               // row i is t_first + i * RL
+    const int hs = R == kSlab ? 0 : half;             // the slab's half (64-row CTAs)
+    const int tb = g * kSlab + hs * R;                // the CTA's first row
+    const int t_first = tb + rl;                      // row i is t_first + i * RL
     // global row t of this rank lives at in_base + t * HD
     const size_t in_base = ((size_t)sl.rk * a.B + sl.b) * L * HD - (size_t)row0 * HD + (size_t)sl.hh * D + c * 8;
     auto valid = [&](int t) { return FULL || (t >= row0 && t < row0 + L); };
@@ -126,12 +138,12 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
         else qmax1 = v;
     }
 #pragma unroll
-    for (int hk = 0; hk < 2; ++hk) {
+    for (int hk = 0; hk < KG; ++hk) {
         Pair16<DT> pr[4];
 #pragma unroll
         for (int x = 0; x < 4; ++x) pr[x].init();
 #pragma unroll
-        for (int i = hk * IT / 2; i < (hk + 1) * IT / 2; ++i) {
+        for (int i = hk * IT / KG; i < (hk + 1) * IT / KG; ++i) {
             const int t = t_first + i * RL;
             // live rows only in the partial live group
             if (FULL || (valid(t) && !(t >= a.used && t / kGK == sl.gu))) {
@@ -156,7 +168,7 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
     qmax0 = warp_max(qmax0);
     if (NQH == 2) qmax1 = warp_max(qmax1);
     kmax0 = warp_max(kmax0);
-    kmax1 = warp_max(kmax1);
+    if (KG == 2) kmax1 = warp_max(kmax1);
     if (lane == 0) {
         sm.red[warp][0] = qmax0;
         sm.red[warp][1] = qmax1;
@@ -174,12 +186,12 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
         qmax0 = warp_max(qmax0);
         if (NQH == 2) qmax1 = warp_max(qmax1);
         kmax0 = warp_max(kmax0);
-        kmax1 = warp_max(kmax1);
+        if (KG == 2) kmax1 = warp_max(kmax1);
         if (lane < NQH) {
             // Q group gg of this lane; its slot range and boundary test
-            const int gg = NQH * g + lane;
-            const bool touched = NQH == 1 || (gg >= sl.fk && gg <= sl.lk);
-            const bool boundary = NQH == 1 ? (sl.js == 0 || sl.js == sl.ts - 1) : (gg == sl.fk || gg == sl.lk);
+            const int gg = (kSlab / GQ) * g + (R / GQ) * hs + lane;
+            const bool touched = GQ == kSlab || (gg >= sl.fk && gg <= sl.lk);
+            const bool boundary = GQ == kSlab ? (sl.js == 0 || sl.js == sl.ts - 1) : (gg == sl.fk || gg == sl.lk);
             float qs = 1.0f;                                 // a half with no row of the rank
             if (touched) {
                 float qam;
@@ -196,8 +208,8 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
                 qs = __fdiv_rn(qam, 127.0f);
             }
             sm.scl[lane] = int8_scale(qs);
-        } else if (lane == 2 || lane == 3) {
-            const int hk = lane - 2, gk = 2 * g + hk;
+        } else if (lane >= 2 && lane < 2 + KG) {
+            const int hk = lane - 2, gk = 2 * g + KG * hs + hk;
             float ks = 1.0f;
             if (gk >= sl.fk && gk <= sl.lk) {
                 const int jk = gk - sl.fk;
@@ -225,16 +237,17 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
         float *qs_out = reinterpret_cast<float *>(chunk + a.lay.qs) + ((size_t)sl.b * a.h + j) * a.nq;
         float *ks_out = reinterpret_cast<float *>(chunk + a.lay.ks) + ((size_t)sl.b * a.h + j) * a.nk;
         const int t = threadIdx.x;
-        if (NQH == 1 && t == 0) qs_out[sl.js] = sm.scl[0].s;
-        if (NQH == 2 && t < 2) {
-            const int gg = 2 * g + t;
+        if (GQ == kSlab && t == 0 && hs == 0) qs_out[sl.js] = sm.scl[0].s;   // one writer per slab
+        if (GQ != kSlab && t < NQH) {
+            const int gg = (kSlab / GQ) * g + (R / GQ) * hs + t;
             if (gg >= sl.fk && gg <= sl.lk) qs_out[gg - sl.fk] = sm.scl[t].s;
         }
-        if (t == 2 || t == 3) {
-            const int gk = 2 * g + (t - 2);
+        if (t >= 2 && t < 2 + KG) {
+            const int gk = 2 * g + KG * hs + (t - 2);
             if (gk >= sl.fk && gk <= sl.lk) ks_out[gk - sl.fk] = sm.scl[t].s;
         }
-        if (sl.js == sl.ts - 1) {                        // slots past the touched groups
+        // slots past the touched groups: the CTA of the slab's last rows
+        if (sl.js == sl.ts - 1 && (R == kSlab || hs == 1)) {
             if (sl.b == a.B - 1 && j == a.h - 1) {
                 // the last writer of the chunk's scale sections zeroes their
                 // alignment padding, so every chunk byte is defined
@@ -244,7 +257,7 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
                 if (nqs + t < (a.lay.ks - a.lay.qs) / 4) qsec[nqs + t] = 0.0f;
                 if (nks + t < (a.lay.bytes - a.lay.ks) / 4) ksec[nks + t] = 0.0f;
             }
-            const int tq = NQH == 1 ? sl.ts : sl.tk;    // touched Q groups
+            const int tq = GQ == kSlab ? sl.ts : sl.tk;  // touched Q groups
             if (tq + t < a.nq) qs_out[tq + t] = __fdiv_rn(kEps, 127.0f);
             if (sl.tk + t < a.nk) {
                 float kam;
@@ -280,12 +293,12 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
         }
     }
     to_f32x8<DT>(*reinterpret_cast<const uint4 *>(a.k_mean + ((size_t)sl.b * a.H + sl.hh) * D + c * 8), m);
-    const bool k_sat = !a.fused || g * kSlab + kSlab > a.used;   // CTA-uniform
+    const bool k_sat = !a.fused || tb + R > a.used;   // CTA-uniform
 #pragma unroll
-    for (int hk = 0; hk < 2; ++hk) {
+    for (int hk = 0; hk < KG; ++hk) {
         const Int8Scale ksc = sm.scl[2 + hk];
 #pragma unroll
-        for (int i = hk * IT / 2; i < (hk + 1) * IT / 2; ++i) {
+        for (int i = hk * IT / KG; i < (hk + 1) * IT / KG; ++i) {
             const int t = t_first + i * RL;
             if (valid(t)) {
                 float f[8];
@@ -318,23 +331,26 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, Pac
     }
 }
 
-// One CTA per slab (blockIdx = head, slab index, rank * B + batch).
-//  1. V rows of the slab -> shared memory with cp.async (each thread later
+// One CTA per slab, or per 64-row half at D = 128 with 64-row Q groups
+// (blockIdx = head, slab index (times 2 plus the half), rank * B + batch).
+//  1. V rows of the CTA -> shared memory with cp.async (each thread later
 //     reads back only the bytes it copied, so no barrier guards them);
-//  2. Q and K rows -> registers; V channel scales and their bracketing
-//     reciprocals -> shared memory (one reciprocal per channel);
-//  3. Q amax and the amax of the two 64-row K groups: per-thread, per-warp,
-//     then warp 0 merges the warps, applies the boundary rules and publishes
-//     the scales;
+//  2. Q and K rows -> registers; V channel scales and their reciprocals ->
+//     shared memory (one reciprocal per channel);
+//  3. Q amax and the amax of the CTA's 64-row K groups: per-thread,
+//     per-warp, then warp 0 merges the warps, applies the boundary rules and
+//     publishes the scales;
 //  4. Q/K codes from the registers; 5. V codes from shared memory.
 template <int D, int DT, int GQ>
-__global__ void __launch_bounds__(pack_threads<D>(), 1024 / pack_threads<D>()) pack_kernel(PackArgs a)
+__global__ void __launch_bounds__(pack_threads<D, GQ>(), 1024 / pack_threads<D, GQ>()) pack_kernel(PackArgs a)
 {
-    __shared__ __align__(16) PackSmem<D> sm;
+    constexpr int R = pack_rows<D, GQ>();
+    __shared__ __align__(16) PackSmem<D, GQ> sm;
     pdl_trigger();
     Slab sl;
     sl.hh = blockIdx.x;
-    sl.js = blockIdx.y;
+    const int hs = R == kSlab ? 0 : (int)(blockIdx.y & 1u);   // the slab's half (64-row CTAs)
+    sl.js = R == kSlab ? (int)blockIdx.y : (int)(blockIdx.y >> 1);
     sl.rk = blockIdx.z / a.B;
     sl.b = blockIdx.z - sl.rk * a.B;
     sl.r = a.rank >= 0 ? a.rank : sl.rk;
@@ -352,10 +368,24 @@ __global__ void __launch_bounds__(pack_threads<D>(), 1024 / pack_threads<D>()) p
     sl.lk = last_group(sl.r, a.L, kGK);
     sl.tk = sl.lk - sl.fk + 1;
     sl.gu = a.used < sl.S ? (a.used - 1) / kGK : -1;
-    const bool full = sl.g * kSlab >= sl.row0 && sl.g * kSlab + kSlab <= sl.row0 + a.L &&
-                      !(sl.gu >= 0 && sl.gu / 2 == sl.g);
-    if (full) pack_slab<D, DT, GQ, true>(a, sl, sm);
-    else pack_slab<D, DT, GQ, false>(a, sl, sm);
+    // FULL: the CTA's rows all belong to the rank and its K groups exclude no
+    // row (written per case: the whole-slab form keeps that kernel free of spills)
+    bool full;
+    if (R == kSlab) {
+        full = sl.g * kSlab >= sl.row0 && sl.g * kSlab + kSlab <= sl.row0 + a.L &&
+               !(sl.gu >= 0 && sl.gu / 2 == sl.g);
+    } else {
+        const int tb = sl.g * kSlab + hs * R;
+        full = tb >= sl.row0 && tb + R <= sl.row0 + a.L && sl.gu != 2 * sl.g + hs;
+    }
+    if (full) pack_slab<D, DT, GQ, true>(a, sl, hs, sm);
+    else pack_slab<D, DT, GQ, false>(a, sl, hs, sm);
+}
+
+template <int D, int DT, int GQ>
+static cudaError_t pack_launch(dim3 grid, cudaStream_t st, bool pdl, const PackArgs &a)
+{
+    return launch_kernel(pack_kernel<D, DT, GQ>, grid, dim3(pack_threads<D, GQ>()), st, pdl, a);
 }
 
 }  // namespace ulp
@@ -384,25 +414,26 @@ extern "C" int ulp_pack(const void *q, const void *k, const void *v, const void 
                used_sequence < 0 ? L * world_size : used_sequence, fused, send_layout,
                slots(L, q_group), slots(L, kGK)};
     // A shard touches at least ceil(L/G) groups, so at most one slot per
-    // (b, head) is untouched; the last slab's CTA writes it.
+    // (b, head) is untouched; the CTA of the last slab's last rows writes it.
     const int nranks = rank == ULP_ALL_RANKS ? world_size : 1;
     const int nslab = slots(L, kSlab);
-    if (nslab > 65535 || (long long)nranks * B > 65535)
+    const int halves = D == 128 && q_group == 64 ? 2 : 1;   // CTAs per slab
+    if ((long long)nslab * halves > 65535 || (long long)nranks * B > 65535)
         return fail(ULP_EINVAL, "pack: grid too large (slabs %d, ranks x batch %lld)", nslab,
                     (long long)nranks * B);
-    const dim3 grid((unsigned)H, (unsigned)nslab, (unsigned)(nranks * B));
+    const dim3 grid((unsigned)H, (unsigned)(nslab * halves), (unsigned)(nranks * B));
     const cudaStream_t st = (cudaStream_t)stream;
     const bool pdl = pdl_enabled(enable_pdl);
     a.early = enable_pdl == 2;
-#define ULP_PACK_LAUNCH(GQ_)                                                                         \
-    do {                                                                                             \
-        if (D == 128) {                                                                              \
-            if (dtype == ULP_BF16) launch_kernel(pack_kernel<128, ULP_BF16, GQ_>, grid, dim3(pack_threads<128>()), st, pdl, a); \
-            else launch_kernel(pack_kernel<128, ULP_FP16, GQ_>, grid, dim3(pack_threads<128>()), st, pdl, a);                   \
-        } else {                                                                                     \
-            if (dtype == ULP_BF16) launch_kernel(pack_kernel<64, ULP_BF16, GQ_>, grid, dim3(pack_threads<64>()), st, pdl, a);  \
-            else launch_kernel(pack_kernel<64, ULP_FP16, GQ_>, grid, dim3(pack_threads<64>()), st, pdl, a);                    \
-        }                                                                                            \
+#define ULP_PACK_LAUNCH(GQ_)                                                                  \
+    do {                                                                                      \
+        if (D == 128) {                                                                       \
+            if (dtype == ULP_BF16) pack_launch<128, ULP_BF16, GQ_>(grid, st, pdl, a);          \
+            else pack_launch<128, ULP_FP16, GQ_>(grid, st, pdl, a);                           \
+        } else {                                                                              \
+            if (dtype == ULP_BF16) pack_launch<64, ULP_BF16, GQ_>(grid, st, pdl, a);           \
+            else pack_launch<64, ULP_FP16, GQ_>(grid, st, pdl, a);                            \
+        }                                                                                     \
     } while (0)
     if (q_group == 128) ULP_PACK_LAUNCH(128);
     else ULP_PACK_LAUNCH(64);
