@@ -1,7 +1,8 @@
 // K grouped amax (page "k_grouped_amax"), the raw-K boundary min/max producer
-// and the boundary derive (page "derive_k_boundary_amax").
+// and the boundary derive (page "derive_k_boundary_amax"); also the optional
+// debug check that the rows past used_sequence are zero.
 //
-// All three are reductions over at most 64 (K) or q_group <= 128 (Q) rows of one head.
+// The first three are reductions over at most 64 (K) or q_group <= 128 (Q) rows of one head.
 // Threads own one 16-byte column vector (8 channels) and a row lane; loads are
 // 16-byte and coalesced along the head's D contiguous elements; the maxima are
 // fp32 fmaxf trees (exact, so order-independent).

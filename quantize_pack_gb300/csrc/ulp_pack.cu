@@ -4,11 +4,12 @@
 // buffer of chunks; Returns: the V scale remains with the caller).
 //
 // Work unit: a "slab" = the rows of one 128-row global group of one head on
-// one rank, one CTA each.  Q and K rows are loaded once into registers, V rows
-// into shared memory; the Q amax (of the slab's one 128-row Q group, or of its
-// two 64-row Q groups when q_group = 64) and the amax of its two 64-row K
-// groups are reduced in the CTA and the codes are written from the same
-// registers.
+// one rank, one CTA each (at D = 128 with q_group = 64, one CTA per 64-row
+// half: one K group and one Q group).  Q and K rows are loaded once into
+// registers, V rows into shared memory; the Q amax (of the slab's one 128-row
+// Q group, or of the 64-row Q groups when q_group = 64) and the amax of the
+// CTA's 64-row K groups are reduced in the CTA and the codes are written from
+// the same registers.
 // Boundary groups (the rank's first/last touched group) take their amax from
 // the gathered partials (Q) or the derived slots (K), so every input byte
 // crosses HBM once.  Quotients use a correctly rounded reciprocal and

@@ -8,7 +8,8 @@
 //    transpose with byte permutes, 16 x 16-byte stores): loads are 64-byte
 //    row segments, stores 128-byte row segments of v8.
 //  - Q/K: each (source, batch) block of L*h*D bytes is one contiguous run on
-//    both sides; blocks copy 16 KiB pieces with 16-byte vectors.
+//    both sides; blocks copy 32 KiB pieces, 16 vectors of 16 bytes in flight
+//    per thread.
 //  - scales: one thread per output slot.
 #include "ulp_internal.cuh"
 
