@@ -1,5 +1,6 @@
 // Host side of the ulp library: status reporting, argument checks, geometry
 // queries and the emulated all-to-all.
+#include <atomic>
 #include <cstring>
 #include <string>
 
@@ -73,15 +74,19 @@ bool pdl_enabled(int enable_pdl)
 {
     if (enable_pdl >= 1) return true;
     if (enable_pdl == 0) return false;
-    static int cached[64];   // per device: 0 unknown, 1 no, 2 yes
+    // per device: 0 unknown, 1 no, 2 yes; every thread computes the same
+    // value, so relaxed atomics suffice
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-    if (cached[dev] == 0) {
+    int c = cached[dev].load(std::memory_order_relaxed);
+    if (c == 0) {
         int major = 0;
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-        cached[dev] = major >= 9 ? 2 : 1;
+        c = major >= 9 ? 2 : 1;
+        cached[dev].store(c, std::memory_order_relaxed);
     }
-    return cached[dev] == 2;
+    return c == 2;
 }
 
 }  // namespace ulp

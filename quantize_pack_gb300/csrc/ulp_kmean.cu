@@ -13,6 +13,8 @@
 // lowest tree levels over them, writing one fp64 node per group of G blocks
 // to the workspace; kernel B (one thread per rank and channel) finishes each
 // rank's tree and the rank sum.  Reads 2 bytes per K element: HBM-bound.
+#include <atomic>
+
 #include "ulp_internal.cuh"
 
 namespace ulp {
@@ -193,11 +195,12 @@ static void launch_blocks(int G, dim3 grid, cudaStream_t st, const KMeanArgs &a)
 // Resident kernel-A CTAs per SM for group G (cached per device and dtype).
 static int resident_ctas(int G, int dtype)
 {
-    static int cache[64][2][4];
+    // every thread computes the same value, so relaxed atomics suffice
+    static std::atomic<int> cache[64][2][4];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
     const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3, di = dtype == ULP_BF16 ? 0 : 1;
-    int &c = cache[dev][di][gi];
+    int c = cache[dev][di][gi].load(std::memory_order_relaxed);
     if (c == 0) {
         int n = 0;
         const void *f = nullptr;
@@ -209,6 +212,7 @@ static int resident_ctas(int G, int dtype)
               : G == 4 ? (const void *)kmean_blocks_kernel<ULP_FP16, 4> : (const void *)kmean_blocks_kernel<ULP_FP16, 8>;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kMeanThreads, 0) != cudaSuccess || n < 1) n = 1;
         c = n;
+        cache[dev][di][gi].store(c, std::memory_order_relaxed);
     }
     return c;
 }
