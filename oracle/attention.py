@@ -1,7 +1,7 @@
 """CPU oracle of the attention that consumes the unpacked tensors.
 
-TEST INFRASTRUCTURE ONLY: imported by tests/ and the bench's CPU legs, never
-by the library; it imports nothing from the CUDA package.
+TEST INFRASTRUCTURE ONLY: imported by tests/ and the smoke check, never by
+the library; it imports nothing from the CUDA package.
 
 Page "flashinfer.comm._ulysses_lowp.unpack_for_sage" hands its outputs to a
 Sage-style attention kernel: INT8 Q/K [B, S, h, D] with FP32 per-group scales
