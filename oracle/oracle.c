@@ -24,10 +24,10 @@
  * first_G(r) = (r*L)/G.
  *
  * Parity status: every function here is pinned by the tests under tests/
- * (test_oracle_*.py); the chunk byte layout, the axis order of the gathered
- * min/max buffer, the Q group width and the V-scale shape are readings of
- * this library (the pages do not fix them) and are pinned only by the
- * round-trip / P-invariance checks.
+ * (test_oracle_*.py).  Parity unpinned: the chunk byte layout, the axis
+ * order of the gathered min/max buffer, the Q group width and the V-scale
+ * shape are readings of this library (the pages do not fix them); they are
+ * checked only indirectly, by the round-trip and P-invariance tests.
  */
 #include <math.h>
 #include <stdint.h>
