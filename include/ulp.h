@@ -66,8 +66,10 @@
  * the groups any rank touches.  Slots past the groups a rank touches hold
  * the floor value 1e-7 (amax) / rn(1e-7/127) (scale).
  *
- * Chunk layout (one source rank -> one destination), each section 16-byte
- * aligned, in this order:
+ * Chunk layout (one source rank -> one destination; page "unpack_for_sage",
+ * recv_u8 parameter: the receiver gets one source-major chunk per source; the
+ * pages do not print the bytes inside a chunk, so this order is a reading of
+ * this library), each section 16-byte aligned, in this order:
  *   Q int8 [B, L, h, D] | K int8 [B, L, h, D] | V e4m3 [B, L, h, D] |
  *   q_scale f32 [B, h, slots(L,q_group)] | k_scale f32 [B, h, slots(L,64)]
  * Chunk p of a source carries global heads [p*h, (p+1)*h).
@@ -223,7 +225,11 @@ int ulp_derive_k_boundary_amax(float *grouped_amax, const float *gathered_minmax
                                const void *k_mean, int dtype, int B, int H, int D, int rank,
                                int local_sequence, int world_size, ulp_stream_t stream);
 
-/* Sender pack of rank r into its P chunks (layout above).
+/* Sender pack of rank r into its P chunks (layout above).  The pages print no
+ * pack step: this is the producer of what page "unpack_for_sage" consumes
+ * (recv_u8: source-major chunks of INT8 Q/K, FP8 E4M3 V and fp32 scales;
+ * Returns: the V scale stays with the caller), with the scales of page
+ * "k_grouped_amax" (Returns) and page "derive_k_boundary_amax".
  *   Q amax of q_group-row group g: max(1e-7, max |f32(q)|) over g's rows; for the
  *   rank's first/last touched Q group it is the max of gathered_q_partial over
  *   the ranks touching g, otherwise computed from the rank's own rows.
