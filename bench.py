@@ -72,8 +72,11 @@ def tensor_peak():
 
 # ------------------------------------------------------- recorded traffic
 
-PACK_SOURCES = ["quantize_pack_gb300/csrc/ulp_pack.cu", "quantize_pack_gb300/csrc/ulp_internal.cuh"]
-TRAFFIC_PROFILE = "profiles/pack_kernel_long_nonaligned.md"
+PACK_SOURCES = ["quantize_pack_gb300/csrc/ulp_pack.cu", "quantize_pack_gb300/csrc/ulp_pack.cuh",
+                "quantize_pack_gb300/csrc/ulp_internal.cuh"]
+# the DRAM bytes of one pack launch, from one ncu capture (written by hand from
+# its output, with the digest of the pack sources it was taken on)
+TRAFFIC_RECORD = "profiles/pack_traffic.json"
 
 
 def pack_source_digest():
@@ -87,22 +90,15 @@ def pack_source_digest():
 
 def recorded_traffic(workload_name):
     """DRAM bytes (read + write) per pack launch from the committed ncu
-    summary, or None when it was taken on other kernel sources or another
+    record, or None when it was taken on other kernel sources or another
     workload."""
-    path = os.path.join(ROOT, TRAFFIC_PROFILE)
     try:
-        fields = {}
-        with open(path) as f:
-            for line in f:
-                if ":" in line and not line.startswith("#"):
-                    k, v = line.split(":", 1)
-                    fields[k.strip().strip("`- ")] = v.strip().strip("`")
-        if fields.get("source_sha256") != pack_source_digest():
+        with open(os.path.join(ROOT, TRAFFIC_RECORD)) as f:
+            rec = json.load(f)
+        if rec.get("source_sha256") != pack_source_digest() or rec.get("workload") != workload_name:
             return None
-        if fields.get("workload") != workload_name:
-            return None
-        return int(fields["traffic_bytes_per_launch"])
-    except (OSError, KeyError, ValueError):
+        return int(rec["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError, TypeError):
         return None
 
 

@@ -233,11 +233,14 @@ int ulp_derive_k_boundary_amax(float *grouped_amax, const float *gathered_minmax
  *   Q amax of q_group-row group g: max(1e-7, max |f32(q)|) over g's rows; for the
  *   rank's first/last touched Q group it is the max of gathered_q_partial over
  *   the ranks touching g, otherwise computed from the rank's own rows.
- *   K amax: k_amax slots.  fused = 0: every slot is read from k_amax (the
- *   output of ulp_k_grouped_amax after ulp_derive_k_boundary_amax).  fused = 1:
- *   only the boundary slots (first/last touched) are read -- they must hold
- *   the derived values -- and the other slots are computed from the rank's own
- *   K rows in the same pass and written to k_amax (same values as fused = 0).
+ *   K amax: k_amax slots.  The boundary slots (the rank's first/last touched
+ *   K groups): with gathered_minmax given, derived in this call from it and
+ *   k_mean by the formula of page "derive_k_boundary_amax" and written to
+ *   k_amax (the values ulp_derive_k_boundary_amax writes); with
+ *   gathered_minmax NULL, read from k_amax, which must then hold the derived
+ *   values.  The other slots: fused = 0: read from k_amax (the output of
+ *   ulp_k_grouped_amax); fused = 1: computed from the rank's own K rows in the
+ *   same pass and written to k_amax (same values as fused = 0).
  *   scale = rn(amax / 127); q8 = sat8(rne(rn(f32(q) / qs))),
  *   k8 = sat8(rne(rn(rn(f32(k) - f32(m)) / ks))),
  *   v8 = e4m3_satfinite_rn(rn(f32(v) / v_scale[b,H,d])).
@@ -245,6 +248,7 @@ int ulp_derive_k_boundary_amax(float *grouped_amax, const float *gathered_minmax
  *   k_mean              [B, H, D] dtype
  *   k_amax              [B, H, slots(L,64)] fp32 ([P, ...] for ULP_ALL_RANKS)
  *   gathered_q_partial  [P, B, H, 2] fp32 (from ulp_boundary_minmax)
+ *   gathered_minmax     [P, B, H, 2, 2, D] fp32 (from ulp_boundary_minmax), or NULL
  *   v_scale             [B, H, D] fp32, the caller's V scale (per global head);
  *                       positive and at least 2^-92 (smaller scales may code
  *                       inputs below 2^-102 with the wrong E4M3 value)
@@ -254,9 +258,10 @@ int ulp_derive_k_boundary_amax(float *grouped_amax, const float *gathered_minmax
  *                       receive buffers of every destination: chunk (r, p) is
  *                       written at [p][r] (the exchange folded into the stores). */
 int ulp_pack(const void *q, const void *k, const void *v, const void *k_mean, int dtype,
-             float *k_amax, const float *gathered_q_partial, const float *v_scale, int B, int L,
-             int H, int D, int rank, int world_size, int used_sequence, int q_group, int fused,
-             uint8_t *send, int send_layout, int enable_pdl, ulp_stream_t stream);
+             float *k_amax, const float *gathered_q_partial, const float *gathered_minmax,
+             const float *v_scale, int B, int L, int H, int D, int rank, int world_size,
+             int used_sequence, int q_group, int fused, uint8_t *send, int send_layout,
+             int enable_pdl, ulp_stream_t stream);
 
 /* The all-to-all, emulated on one GPU: recv[p][s] = send[s][p] for the
  * [P, P, chunk_bytes] buffers of all ranks (page "unpack_for_sage": recv_u8 is

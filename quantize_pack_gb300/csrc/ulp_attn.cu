@@ -520,25 +520,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 // ------------------------------------------------------------ host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled()
-{
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
 // fp16 tensor [planes, rows, cols] (cols contiguous) as a 3-D map with
 // boxes of 64 columns x box_rows rows and the 128-byte swizzle.
 int make_map(CUtensorMap *m, void *base, uint64_t cols, uint64_t rows, uint64_t planes, uint32_t box_rows)

@@ -2,6 +2,7 @@
 // queries and the emulated all-to-all.
 #include <atomic>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "ulp_internal.cuh"
@@ -26,6 +27,21 @@ int check_launch(const char *what)
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(ULP_ECUDA, "%s: %s", what, cudaGetErrorString(e));
     return ULP_OK;
+}
+
+EncodeTiledFn encode_tiled()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
 }
 
 bool aligned16(const void *p) { return p != nullptr && ((uintptr_t)p & 15u) == 0; }

@@ -2,6 +2,7 @@
 // conversions and reductions.  Not part of the ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -53,6 +54,15 @@ __host__ __device__ __forceinline__ ChunkLayout chunk_layout(int B, int L, int h
     c.bytes = c.ks + align16(sizeof(float) * (size_t)B * h * slots(L, kGK));
     return c;
 }
+
+// ------------------------------------------------------ device properties
+
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point
+// (the library does not link libcuda); null when the driver lacks it.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled();
 
 // ---------------------------------------------------------- argument checks
 

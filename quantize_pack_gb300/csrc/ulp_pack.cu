@@ -15,22 +15,9 @@
 // crosses HBM once.  Quotients use a correctly rounded reciprocal and
 // Markstein's correction (ulp_internal.cuh), so the codes are those of the
 // IEEE quotient.
-#include "ulp_internal.cuh"
+#include "ulp_pack.cuh"
 
 namespace ulp {
-
-struct PackArgs {
-    const uint16_t *q, *k, *v, *k_mean;
-    float *k_amax;
-    const float *qpart;    // [P, B, H, 2]
-    const float *v_scale;  // [B, H, D]
-    uint8_t *send;
-    ChunkLayout lay;
-    int B, L, H, P, h, rank, used, fused, layout, nq, nk;   // nq = slots(L, q_group)
-    int early;   // read q, k, v, k_mean, v_scale before waiting for the preceding kernel
-};
-
-constexpr int kSlab = 128;   // rows of a slab: one 128-row group = two 64-row groups
 
 // Rows per CTA: a whole slab, or at D = 128 with 64-row Q groups one 64-row
 // half (one K group, one Q group), so that four CTAs stay resident per SM.
@@ -180,6 +167,19 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, int
 
     const size_t amax_row = (((size_t)sl.rk * a.B + sl.b) * a.H + sl.hh) * a.nk;
     if (warp == 0) {
+        // the rank's first/last K groups in this CTA, derived from the
+        // gathered raw-K min/max when they are given (all 32 lanes)
+        float kder[2] = {0.0f, 0.0f};
+        if (a.gathered) {
+#pragma unroll
+            for (int hk = 0; hk < KG; ++hk) {
+                const int gk = 2 * g + KG * hs + hk;
+                if (gk >= sl.fk && gk <= sl.lk && (gk == sl.fk || gk == sl.lk)) {
+                    kder[hk] = derive_slot_warp<D, DT>(a.gathered, a.k_mean, a.B, a.H, L, a.P, sl.b, sl.hh, gk);
+                    if (lane == 0) a.k_amax[amax_row + (gk - sl.fk)] = kder[hk];
+                }
+            }
+        }
         qmax0 = lane < NW ? sm.red[lane][0] : -INFINITY;
         qmax1 = lane < NW ? sm.red[lane][1] : -INFINITY;
         kmax0 = lane < NW ? sm.red[lane][2] : -INFINITY;
@@ -215,7 +215,9 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, int
             if (gk >= sl.fk && gk <= sl.lk) {
                 const int jk = gk - sl.fk;
                 float kam;
-                if (jk == 0 || jk == sl.tk - 1 || !a.fused) {
+                if ((jk == 0 || jk == sl.tk - 1) && a.gathered) {
+                    kam = kder[hk];
+                } else if (jk == 0 || jk == sl.tk - 1 || !a.fused) {
                     kam = a.k_amax[amax_row + jk];
                 } else {
                     kam = floor_eps(hk == 0 ? kmax0 : kmax1);
@@ -394,10 +396,10 @@ static cudaError_t pack_launch(dim3 grid, cudaStream_t st, bool pdl, const PackA
 using namespace ulp;
 
 extern "C" int ulp_pack(const void *q, const void *k, const void *v, const void *k_mean, int dtype,
-                        float *k_amax, const float *gathered_q_partial, const float *v_scale, int B,
-                        int L, int H, int D, int rank, int world_size, int used_sequence,
-                        int q_group, int fused, uint8_t *send, int send_layout, int enable_pdl,
-                        ulp_stream_t stream)
+                        float *k_amax, const float *gathered_q_partial, const float *gathered_minmax,
+                        const float *v_scale, int B, int L, int H, int D, int rank, int world_size,
+                        int used_sequence, int q_group, int fused, uint8_t *send, int send_layout,
+                        int enable_pdl, ulp_stream_t stream)
 {
     if (int s = check_common(dtype, B, L, H, D, rank, world_size, used_sequence, enable_pdl)) return s;
     if (int s = check_q_group(q_group, "pack")) return s;
@@ -405,12 +407,13 @@ extern "C" int ulp_pack(const void *q, const void *k, const void *v, const void 
     if (send_layout != ULP_SEND_SOURCE_MAJOR && send_layout != ULP_SEND_DEST_MAJOR)
         return fail(ULP_EINVAL, "pack: send_layout must be 0 or 1 (got %d)", send_layout);
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(k_mean) || !aligned4(k_amax) ||
-        !aligned4(gathered_q_partial) || !aligned16(v_scale) || !aligned16(send))
+        !aligned4(gathered_q_partial) || !aligned16(v_scale) || !aligned16(send) ||
+        (gathered_minmax && !aligned4(gathered_minmax)))
         return fail(ULP_EALIGN, "pack: q, k, v, k_mean, v_scale, send must be 16-byte aligned, "
-                                "k_amax and gathered_q_partial 4-byte aligned");
+                                "k_amax, gathered_q_partial and gathered_minmax 4-byte aligned");
     const int h = H / world_size;
     PackArgs a{(const uint16_t *)q, (const uint16_t *)k, (const uint16_t *)v, (const uint16_t *)k_mean,
-               k_amax, gathered_q_partial, v_scale, send, chunk_layout(B, L, h, D, q_group),
+               k_amax, gathered_q_partial, gathered_minmax, v_scale, send, chunk_layout(B, L, h, D, q_group),
                B, L, H, world_size, h, rank,
                used_sequence < 0 ? L * world_size : used_sequence, fused, send_layout,
                slots(L, q_group), slots(L, kGK)};

@@ -8,10 +8,11 @@ CUDA graph.
 All P shards sit in device memory; the stats all-gather is the stacked
 [P, ...] buffer the boundary kernel writes, and the all-to-all is folded into
 the pack's store addresses (dest-major send buffer = every destination's
-recv_u8) or, on request, run as a separate device copy.  One step is four
-launches of the CUDA library: boundary min/max -> derive -> pack -> unpack
-(plus k_grouped_amax when the unfused pack is chosen, plus the copy when the
-exchange is not folded).
+recv_u8) or, on request, run as a separate device copy.  One step is three
+launches of the CUDA library: boundary min/max -> pack (which derives the K
+boundary slots from the gathered min/max itself) -> unpack; plus derive when
+``fold_derive`` is off, k_grouped_amax when the unfused pack is chosen, and
+the copy when the exchange is not folded.
 """
 from __future__ import annotations
 
@@ -26,7 +27,7 @@ class UlyssesLowpPath:
     def __init__(self, *, B: int, L: int, H: int, D: int, world_size: int, dtype: torch.dtype,
                  used_sequence: Optional[int] = None, scale_sequence: Optional[int] = None,
                  aligned: Optional[bool] = None, q_group: int = ulp.GQ, fused: bool = True,
-                 fold_exchange: bool = True,
+                 fold_exchange: bool = True, fold_derive: bool = True,
                  pdl: Optional[bool] = None, pdl_unpack: Optional[bool] = None, device="cuda"):
         P = world_size
         self.B, self.L, self.H, self.D, self.P = B, L, H, D, P
@@ -39,8 +40,10 @@ class UlyssesLowpPath:
         self.q_group = q_group
         self.fused = fused
         self.fold_exchange = fold_exchange
-        # pdl: programmatic launch of pack, which follows derive (derive writes
-        # none of pack's inputs, so pack loads them before waiting);
+        self.fold_derive = fold_derive
+        # pdl: programmatic launch of pack, which follows the boundary min/max
+        # (or derive); neither writes pack's inputs, so pack loads them before
+        # waiting;
         # pdl_unpack: of unpack (default off: its early CTAs would sit on SMs
         # through pack's last wave)
         self.pdl_pack = 2 if pdl is None or pdl else 0
@@ -59,7 +62,7 @@ class UlyssesLowpPath:
 
     @property
     def launches_per_step(self) -> int:
-        return 4 + (0 if self.fused else 1)
+        return 3 + (0 if self.fold_derive else 1) + (0 if self.fused else 1)
 
     @property
     def copies_per_step(self) -> int:
@@ -79,18 +82,16 @@ class UlyssesLowpPath:
                                used_sequence=self.used_sequence, out=self.k_amax)
         ulp.boundary_minmax(k, q, rank=None, world_size=P, used_sequence=self.used_sequence,
                             q_group=self.q_group, out=(self.minmax, self.q_partial))
-        ulp.derive_k_boundary_amax(self.k_amax, self.minmax, k_mean, rank=None, local_sequence=L,
-                                   world_size=P)
+        if not self.fold_derive:
+            ulp.derive_k_boundary_amax(self.k_amax, self.minmax, k_mean, rank=None, local_sequence=L,
+                                       world_size=P)
         if on_pack is not None:
             on_pack[0]()
-        if self.fold_exchange:
-            ulp.pack(q, k, v, k_mean, self.k_amax, self.q_partial, v_scale, rank=None,
-                     world_size=P, used_sequence=self.used_sequence, q_group=self.q_group,
-                     fused=self.fused, send=self.recv, send_layout=ulp.SEND_DEST_MAJOR, enable_pdl=self.pdl_pack)
-        else:
-            ulp.pack(q, k, v, k_mean, self.k_amax, self.q_partial, v_scale, rank=None,
-                     world_size=P, used_sequence=self.used_sequence, q_group=self.q_group,
-                     fused=self.fused, send=self.send, send_layout=ulp.SEND_SOURCE_MAJOR, enable_pdl=self.pdl_pack)
+        ulp.pack(q, k, v, k_mean, self.k_amax, self.q_partial, v_scale, rank=None,
+                 world_size=P, used_sequence=self.used_sequence, q_group=self.q_group,
+                 fused=self.fused, send=self.recv if self.fold_exchange else self.send,
+                 send_layout=ulp.SEND_DEST_MAJOR if self.fold_exchange else ulp.SEND_SOURCE_MAJOR,
+                 gathered_minmax=self.minmax if self.fold_derive else None, enable_pdl=self.pdl_pack)
         if on_pack is not None:
             on_pack[1]()
         if not self.fold_exchange:

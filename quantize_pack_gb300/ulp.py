@@ -65,8 +65,8 @@ def lib() -> ctypes.CDLL:
         L.ulp_boundary_minmax.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]
         L.ulp_derive_k_boundary_amax.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]
         L.ulp_check_padding.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P]
-        L.ulp_pack.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
-                               _P, _I, _I, _P]
+        L.ulp_pack.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                               _I, _P, _I, _I, _P]
         L.ulp_alltoall_emulate.argtypes = [_P, _P, _I, _SZ, _P]
         L.ulp_unpack_for_sage.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                                           _I, _I, _P]
@@ -295,9 +295,14 @@ def pack(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, k_mean_global: torch
          k_amax: torch.Tensor, gathered_q_partial: torch.Tensor, v_scale: torch.Tensor, *,
          rank: Optional[int], world_size: int, used_sequence: Optional[int] = None,
          q_group: int = GQ, fused: bool = True, send: Optional[torch.Tensor] = None,
-         send_layout: int = SEND_SOURCE_MAJOR,
+         send_layout: int = SEND_SOURCE_MAJOR, gathered_minmax: Optional[torch.Tensor] = None,
          enable_pdl=None) -> torch.Tensor:
-    """Quantise a rank's Q/K/V into its P chunks (INT8 Q/K, FP8 E4M3 V)."""
+    """Quantise a rank's Q/K/V into its P chunks (INT8 Q/K, FP8 E4M3 V).
+
+    With ``gathered_minmax`` (the [P, B, H, 2, 2, D] output of
+    ``boundary_minmax``) the K boundary slots are derived inside the pack and
+    written to ``k_amax`` (what ``derive_k_boundary_amax`` would write);
+    without it they are read from ``k_amax``."""
     rc, nr, B, L, H, D = _rank_dims(q, rank)
     h = H // world_size
     cb = chunk_bytes(B, L, h, D, q_group)
@@ -308,7 +313,9 @@ def pack(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, k_mean_global: torch
             shape = ((nr,) if rank is None else ()) + (world_size, cb)
         send = torch.empty(shape, dtype=torch.uint8, device=q.device)
     _check(lib().ulp_pack(_ptr(q), _ptr(k), _ptr(v), _ptr(k_mean_global), _dtype_code(q),
-                          _ptr(k_amax), _ptr(gathered_q_partial), _ptr(v_scale), B, L, H, D, rc,
+                          _ptr(k_amax), _ptr(gathered_q_partial),
+                          None if gathered_minmax is None else _ptr(gathered_minmax),
+                          _ptr(v_scale), B, L, H, D, rc,
                           world_size, _opt(used_sequence), q_group, int(bool(fused)), _ptr(send),
                           int(send_layout), _pdl(enable_pdl), _stream(q.device)))
     return send

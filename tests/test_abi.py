@@ -119,10 +119,12 @@ def test_unpack_rejects(lib):
 def test_pack_and_derive_reject(lib):
     base = [FAKE] * 8
     # fused must be 0/1, send_layout 0/1, q_group 64/128
-    assert lib.ulp_pack(*base[:4], 0, *base[4:7], 1, 96, 8, 64, 0, 2, -1, 128, 2, FAKE, 0, -1, None) == -1
-    assert lib.ulp_pack(*base[:4], 0, *base[4:7], 1, 96, 8, 64, 0, 2, -1, 128, 1, FAKE, 3, -1, None) == -1
-    assert lib.ulp_pack(*base[:4], 0, *base[4:7], 1, 96, 8, 64, 0, 2, -1, 128, 1, FAKE + 2, 0, -1, None) == -3
-    assert lib.ulp_pack(*base[:4], 0, *base[4:7], 1, 96, 8, 64, 0, 2, -1, 32, 1, FAKE, 0, -1, None) == -1
+    assert lib.ulp_pack(*base[:4], 0, *base[4:6], None, base[6], 1, 96, 8, 64, 0, 2, -1, 128, 2, FAKE, 0, -1, None) == -1
+    assert lib.ulp_pack(*base[:4], 0, *base[4:6], None, base[6], 1, 96, 8, 64, 0, 2, -1, 128, 1, FAKE, 3, -1, None) == -1
+    assert lib.ulp_pack(*base[:4], 0, *base[4:6], None, base[6], 1, 96, 8, 64, 0, 2, -1, 128, 1, FAKE + 2, 0, -1, None) == -3
+    assert lib.ulp_pack(*base[:4], 0, *base[4:6], None, base[6], 1, 96, 8, 64, 0, 2, -1, 32, 1, FAKE, 0, -1, None) == -1
+    # a misaligned gathered min/max buffer (the folded derive's input)
+    assert lib.ulp_pack(*base[:4], 0, *base[4:6], FAKE + 2, base[6], 1, 96, 8, 64, 0, 2, -1, 128, 1, FAKE, 0, -1, None) == -3
     assert lib.ulp_derive_k_boundary_amax(FAKE, FAKE, FAKE, 1, 1, 8, 64, 2, 96, 2, None) == -1
     assert lib.ulp_boundary_minmax(FAKE, FAKE, 0, 1, 96, 8, 64, 0, 2, 500, 128, FAKE, FAKE, None) == -1
     assert lib.ulp_boundary_minmax(FAKE, FAKE, 0, 1, 96, 8, 64, 0, 2, -1, 0, FAKE, FAKE, None) == -1

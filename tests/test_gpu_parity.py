@@ -61,33 +61,46 @@ def test_derive(wl):
         gh.assert_bits_equal(one, res["amax"][r], f"derived amax rank {r}")
 
 
+@pytest.mark.parametrize("derive", ["separate", "folded"])
 @pytest.mark.parametrize("fused", [True, False], ids=["fused", "unfused"])
 @pytest.mark.parametrize("wl", GPU_WORKLOADS, ids=lambda w: w.name)
-def test_pack(wl, fused):
+def test_pack(wl, fused, derive):
+    """Pack against the oracle: the chunk bytes (source-major, dest-major,
+    one rank) and k_amax.  derive = "separate": derive_k_boundary_amax runs
+    first and pack reads the boundary slots; "folded": pack derives them from
+    the gathered min/max itself and writes them to k_amax."""
     inp, res, (q, k, v, km, vs) = _setup(wl)
     P = wl.P
+    folded = derive == "folded"
     if fused:
-        # only the derived boundary slots are read; poison the rest
+        # the slots pack must not read are poisoned
         ga = torch.full((P, wl.B, wl.H, ulp.slots(wl.L, 64)), float("nan"), device="cuda")
     else:
         ga = ulp.k_grouped_amax(k, km, rank=None, world_size=P, used_sequence=wl.used_sequence)
     mm, qp = ulp.boundary_minmax(k, q, rank=None, world_size=P, used_sequence=wl.used_sequence,
                                  q_group=wl.q_group)
-    ulp.derive_k_boundary_amax(ga, mm, km, rank=None, local_sequence=wl.L, world_size=P)
+    ga0 = ga.clone()
+    if not folded:
+        ulp.derive_k_boundary_amax(ga, mm, km, rank=None, local_sequence=wl.L, world_size=P)
+    extra = dict(gathered_minmax=mm if folded else None)
     send = ulp.pack(q, k, v, km, ga, qp, vs, rank=None, world_size=P,
-                    used_sequence=wl.used_sequence, q_group=wl.q_group, fused=fused)
+                    used_sequence=wl.used_sequence, q_group=wl.q_group, fused=fused, **extra)
     gh.assert_bits_equal(send, res["send"], "send (source-major)")
     gh.assert_bits_equal(ga, res["amax"], "k_amax after pack")
+    if folded:
+        ga.copy_(ga0)
     recv = ulp.pack(q, k, v, km, ga, qp, vs, rank=None, world_size=P,
                     used_sequence=wl.used_sequence, q_group=wl.q_group, fused=fused,
-                    send_layout=ulp.SEND_DEST_MAJOR)
+                    send_layout=ulp.SEND_DEST_MAJOR, **extra)
     gh.assert_bits_equal(recv, res["recv"], "send (dest-major) = recv")
     # single-rank calls write the same chunks
     r = P - 1
+    one_amax = (ga0 if folded else ga)[r].contiguous()
     one = ulp.pack(q[r].contiguous(), k[r].contiguous(), v[r].contiguous(), km,
-                   ga[r].contiguous(), qp, vs, rank=r, world_size=P,
-                   used_sequence=wl.used_sequence, q_group=wl.q_group, fused=fused)
+                   one_amax, qp, vs, rank=r, world_size=P,
+                   used_sequence=wl.used_sequence, q_group=wl.q_group, fused=fused, **extra)
     gh.assert_bits_equal(one, res["send"][r], f"send rank {r}")
+    gh.assert_bits_equal(one_amax, res["amax"][r], f"k_amax rank {r} after pack")
 
 
 @pytest.mark.parametrize("wl", GPU_WORKLOADS, ids=lambda w: w.name)
