@@ -1,10 +1,15 @@
 """Throughput of the Ulysses low-precision quantize -> pack -> unpack path.
 
-A step is one pass of the whole path (boundary min/max, derive, fused
-amax+pack with the exchange folded into its stores, unpack) over every rank of
-an emulated Ulysses group held on one GPU, on seeded synthetic inputs shaped
-like the long non-aligned workload (B=1, H=40, D=128, P=8, L=9360, bf16,
-used 74800).  Prints one JSON line.
+A step is one pass of the whole path (boundary min/max, then pack with the
+boundary derive and the amax fused in and the exchange folded into its
+stores, then unpack) over every rank of an emulated Ulysses group held on one
+GPU, on seeded synthetic inputs shaped like the long non-aligned workload
+(B=1, H=40, D=128, P=8, L=9360, bf16, used 74800).  Prints one JSON line.
+
+Workloads whose inputs fit in a few times the L2 (``--workload`` tiny or
+padding) are launch-bound: their line also times the step four ways (eager
+launches or one CUDA-graph replay, L2 flushed before each step or not), and
+``value`` is the eager step with the L2 flushed before it.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -42,6 +47,8 @@ def parse():
     ap.add_argument("--mode", choices=["fused", "unfused"], default="fused")
     ap.add_argument("--q-group", type=int, choices=[64, 128], default=128,
                     help="Q group rows (64: Q groups are the K groups)")
+    ap.add_argument("--derive", choices=["folded", "separate"], default="folded",
+                    help="boundary derive inside pack (three launches) or its own launch (four)")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum CPU time spent on the oracle baseline sample")
@@ -273,6 +280,49 @@ def whole_job_value(step_bytes, world, ms):
 
 # ------------------------------------------------------------------ GPU arm
 
+def step_modes(torch, path, inputs, stream, dev, steps, l2_bytes):
+    """The step of a launch-bound workload timed four ways: eager launches or
+    the replay of one captured CUDA graph; with the L2 flushed before each
+    step (a write of twice the L2 size, outside the timed events; median of
+    per-step events) or hot (back-to-back steps in one event pair; mean).
+    Returns {mode: {"ms": ...}}."""
+    flush = torch.empty(max(2 * l2_bytes, 1 << 20), dtype=torch.uint8, device=dev)
+    graph = path.capture(*inputs)
+
+    def eager():
+        path.run(*inputs)
+
+    def replay():
+        graph.replay()
+
+    out = {}
+    for name, run in (("eager", eager), ("graph", replay)):
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[f"{name}_hot"] = {"ms": e0.elapsed_time(e1) / steps}
+        evs = []
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            run()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        out[f"{name}_cold"] = {"ms": statistics.median(a.elapsed_time(b) for a, b in evs)}
+    for v in out.values():
+        v["launches"] = path.launches_per_step
+    del flush
+    return out
+
+
 def run_ours(args, wl, rank, world, dist):
     import numpy as np
     import torch
@@ -296,7 +346,7 @@ def run_ours(args, wl, rank, world, dist):
     path = UlyssesLowpPath(B=wl.B, L=wl.L, H=wl.H, D=wl.D, world_size=wl.P, dtype=dt,
                            used_sequence=wl.used_sequence, scale_sequence=wl.scale_sequence,
                            aligned=wl.aligned, q_group=wl.q_group, fused=(args.mode == "fused"),
-                           fold_exchange=True, device=dev)
+                           fold_exchange=True, fold_derive=(args.derive == "folded"), device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def barrier():
@@ -342,6 +392,30 @@ def run_ours(args, wl, rank, world, dist):
     pack_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev_pack)
     unpack_ms = statistics.mean(e1.elapsed_time(e2) for (_, e1), e2 in zip(ev_pack, ev_end))
     ms, pack_ms, unpack_ms = max_over_ranks(dist, [ms, pack_ms, unpack_ms], dev)
+
+    # ---- launch-bound workloads: eager vs graph replay, cold vs hot L2
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 0)
+    small = 6 * wl.N <= 4 * max(l2_bytes, 1)
+    modes = None
+    if small:
+        modes = step_modes(torch, path, (q, k, v, km, vs), stream, dev, max(K, 50), l2_bytes)
+        (cold_ms,) = max_over_ranks(dist, [modes["eager_cold"]["ms"]], dev)
+
+    # ---- the emulated all-to-all on its own (the step folds it into pack's
+    # stores): the permutation copy recv[p][s] = send[s][p] of every chunk
+    a2a_src, a2a_dst = torch.empty_like(path.recv), torch.empty_like(path.recv)
+    for _ in range(3):
+        ulp.alltoall_emulate(a2a_src, a2a_dst)
+    ta0, ta1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    KX = max(10, K // 10)
+    ta0.record(stream)
+    for _ in range(KX):
+        ulp.alltoall_emulate(a2a_src, a2a_dst)
+    ta1.record(stream)
+    torch.cuda.synchronize()
+    a2a_ms = ta0.elapsed_time(ta1) / KX
+    a2a_bytes = 2 * a2a_src.numel()
+    del a2a_src, a2a_dst
 
     # ---- the step before the path: k_mean_global production (not in the step)
     kmean_out = torch.empty_like(km)
@@ -429,21 +503,29 @@ def run_ours(args, wl, rank, world, dist):
     if rank != 0:
         return
     step_bytes = metrics.step_bytes(wl)
-    value = whole_job_value(step_bytes, world, ms)
+    vms = cold_ms if small else ms          # the step time that value reports
+    value = whole_job_value(step_bytes, world, vms)
     peak, peak_kind = peaks()
+    mhz = clocks.get("sm_mhz") or None
+
+    def cycles(t_ms):
+        """The kernel time in SM clock cycles at the median clock of the
+        timed region (for comparing runs whose clocks differ)."""
+        return None if mhz is None else t_ms * 1e-3 * mhz * 1e6
     pack_gbs = metrics.pack_bytes(wl) / (pack_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": vms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {
             "workload": wl.name, **{k_: v_ for k_, v_ in wl.describe().items() if k_ != "workload"},
             "path": f"{args.mode} amax+pack (exchange folded into the stores) + unpack, "
                     f"{path.launches_per_step} launches/step",
-            "l2": f"inputs {6 * wl.N / 1e9:.2f} GB > 129 MB L2; no flush",
+            "l2": (f"value: L2 ({l2_bytes / 1e6:.0f} MB) flushed before each timed step (a {2 * l2_bytes / 1e6:.0f} MB "
+                   f"write, not timed)" if small else f"inputs {6 * wl.N / 1e9:.2f} GB > 129 MB L2; no flush"),
             "parallelism": f"{world} independent replica(s) of a P={wl.P} emulated Ulysses group",
         },
-        "tokens_per_s": wl.tokens * world / (ms * 1e-3),
+        "tokens_per_s": wl.tokens * world / (vms * 1e-3),
         "hbm_frac": value / world / peak,
         "step_bytes": step_bytes,
         "roofline": {"bound": "hbm", "kernel": "pack_kernel", "achieved": pack_gbs, "peak": peak,
@@ -457,20 +539,28 @@ def run_ours(args, wl, rank, world, dist):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "kernels": {
             "pack": {"ms": pack_ms, "gbs": pack_gbs, "frac": pack_gbs / peak,
-                     "algorithmic_bytes": metrics.pack_bytes(wl)},
+                     "algorithmic_bytes": metrics.pack_bytes(wl), "sm_cycles": cycles(pack_ms)},
             "unpack": {"ms": unpack_ms,
                        "gbs": metrics.unpack_bytes(wl) / (unpack_ms * 1e-3) / 1e9,
                        "frac": metrics.unpack_bytes(wl) / (unpack_ms * 1e-3) / 1e9 / peak,
-                       "algorithmic_bytes": metrics.unpack_bytes(wl)},
-            "boundary_minmax+derive": {"ms": max(0.0, ms - pack_ms - unpack_ms)},
-            "note": "CUDA events around each launch inside the timed steps (means)",
+                       "algorithmic_bytes": metrics.unpack_bytes(wl), "sm_cycles": cycles(unpack_ms)},
+            "boundary_minmax" + ("" if path.fold_derive else "+derive"): {
+                "ms": max(0.0, ms - pack_ms - unpack_ms), "sm_cycles": cycles(max(0.0, ms - pack_ms - unpack_ms))},
+            "note": "CUDA events around each launch inside the timed steps (means); sm_cycles = "
+                    "ms x the median SM clock sampled in the timed region",
         },
+        "alltoall_emulate": {"ms": a2a_ms, "calls": KX, "bytes": a2a_bytes,
+                             "gbs": a2a_bytes / (a2a_ms * 1e-3) / 1e9,
+                             "frac": a2a_bytes / (a2a_ms * 1e-3) / 1e9 / peak, "sm_cycles": cycles(a2a_ms),
+                             "note": "the emulated all-to-all as its own device copy (read + write of "
+                                     "every chunk, 6N bytes); the step folds it into pack's stores; "
+                                     "not in value"},
         "gpu_launches": K * path.launches_per_step,
-        "k_mean_global": {"ms": kmean_ms, "steps": KM,
+        "k_mean_global": {"ms": kmean_ms, "steps": KM, "sm_cycles": cycles(kmean_ms),
                           "achieved_gbs": 2 * wl.N / (kmean_ms * 1e-3) / 1e9,
                           "frac": 2 * wl.N / (kmean_ms * 1e-3) / 1e9 / peak,
                           "note": "the step before the path (reads K once); not in value"},
-        "k_grouped_amax": {"ms": kgamax_ms, "calls": KM,
+        "k_grouped_amax": {"ms": kgamax_ms, "calls": KM, "sm_cycles": cycles(kgamax_ms),
                            "achieved_gbs": 2 * wl.N / (kgamax_ms * 1e-3) / 1e9,
                            "frac": 2 * wl.N / (kgamax_ms * 1e-3) / 1e9 / peak,
                            "note": "the standalone call over all ranks (2N bytes: K read once); "
@@ -485,6 +575,9 @@ def run_ours(args, wl, rank, world, dist):
                               "not in value"},
         "clocks": clocks,
     }
+    if small:
+        line["step_modes"] = modes
+        line["hot_eager_ms_per_step"] = ms
     if not args.no_cpu_baseline:
         run, nbytes, swl = oracle_sample(wl)
         n, t = 0, time.perf_counter()
