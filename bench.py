@@ -1,8 +1,8 @@
 """Throughput of the Ulysses low-precision quantize -> pack -> unpack path.
 
-A step is one pass of the whole path (boundary min/max, then pack with the
-boundary derive and the amax fused in and the exchange folded into its
-stores, then unpack) over every rank of an emulated Ulysses group held on one
+A step is one pass of the whole path (boundary min/max, derive, then pack
+with the amax fused in and the exchange folded into its stores, then unpack;
+launch-bound workloads fold the derive into pack too) over every rank of an emulated Ulysses group held on one
 GPU, on seeded synthetic inputs shaped like the long non-aligned workload
 (B=1, H=40, D=128, P=8, L=9360, bf16, used 74800).  Prints one JSON line.
 
@@ -47,8 +47,9 @@ def parse():
     ap.add_argument("--mode", choices=["fused", "unfused"], default="fused")
     ap.add_argument("--q-group", type=int, choices=[64, 128], default=128,
                     help="Q group rows (64: Q groups are the K groups)")
-    ap.add_argument("--derive", choices=["folded", "separate"], default="folded",
-                    help="boundary derive inside pack (three launches) or its own launch (four)")
+    ap.add_argument("--derive", choices=["auto", "folded", "separate"], default="auto",
+                    help="boundary derive inside pack (three launches) or its own launch (four); "
+                         "auto: inside pack for launch-bound workloads")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum CPU time spent on the oracle baseline sample")
@@ -346,7 +347,8 @@ def run_ours(args, wl, rank, world, dist):
     path = UlyssesLowpPath(B=wl.B, L=wl.L, H=wl.H, D=wl.D, world_size=wl.P, dtype=dt,
                            used_sequence=wl.used_sequence, scale_sequence=wl.scale_sequence,
                            aligned=wl.aligned, q_group=wl.q_group, fused=(args.mode == "fused"),
-                           fold_exchange=True, fold_derive=(args.derive == "folded"), device=dev)
+                           fold_exchange=True, fold_derive={"auto": None, "folded": True, "separate": False}[args.derive],
+                           device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def barrier():

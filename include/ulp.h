@@ -265,7 +265,9 @@ int ulp_pack(const void *q, const void *k, const void *v, const void *k_mean, in
 
 /* The all-to-all, emulated on one GPU: recv[p][s] = send[s][p] for the
  * [P, P, chunk_bytes] buffers of all ranks (page "unpack_for_sage": recv_u8 is
- * the source-major buffer received by all-to-all). */
+ * the source-major buffer received by all-to-all), as one copy kernel.
+ * chunk_bytes is a positive multiple of 16; send and recv must not overlap
+ * (the same pointer gives ULP_EINVAL). */
 int ulp_alltoall_emulate(const uint8_t *send, uint8_t *recv, int world_size, size_t chunk_bytes,
                          ulp_stream_t stream);
 

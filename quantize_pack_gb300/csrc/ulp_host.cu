@@ -1,5 +1,6 @@
 // Host side of the ulp library: status reporting, argument checks, geometry
 // queries and the emulated all-to-all.
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -10,6 +11,36 @@
 namespace ulp {
 
 static thread_local std::string g_last_error;
+
+// ------------------------------------------------------ emulated all-to-all
+
+constexpr int kA2AThreads = 256;
+constexpr int kA2AVecs = 4;   // 16-byte vectors in flight per thread
+
+// recv[p][s] = send[s][p] over [P][P][chunk] buffers: blockIdx.y = p * P + s
+// picks the destination chunk; the x blocks stride over its 16-byte vectors,
+// each thread with kA2AVecs loads in flight before its stores.
+__global__ void __launch_bounds__(kA2AThreads) alltoall_kernel(const uint4 *__restrict__ send,
+                                                                 uint4 *__restrict__ recv, int P, size_t vecs)
+{
+    const int p = blockIdx.y / P, s = blockIdx.y - p * P;
+    const uint4 *src = send + ((size_t)s * P + p) * vecs;
+    uint4 *dst = recv + (size_t)blockIdx.y * vecs;
+    const size_t step = (size_t)gridDim.x * kA2AThreads * kA2AVecs;
+    for (size_t base = (size_t)blockIdx.x * kA2AThreads * kA2AVecs + threadIdx.x; base < vecs; base += step) {
+        uint4 v[kA2AVecs];
+#pragma unroll
+        for (int i = 0; i < kA2AVecs; ++i) {
+            const size_t j = base + (size_t)i * kA2AThreads;
+            if (j < vecs) v[i] = ld_stream(src + j);
+        }
+#pragma unroll
+        for (int i = 0; i < kA2AVecs; ++i) {
+            const size_t j = base + (size_t)i * kA2AThreads;
+            if (j < vecs) dst[j] = v[i];
+        }
+    }
+}
 
 int fail(int status, const char *fmt, ...)
 {
@@ -159,17 +190,14 @@ int ulp_alltoall_emulate(const uint8_t *send, uint8_t *recv, int world_size, siz
     if (chunk_bytes == 0 || chunk_bytes % 16 != 0)
         return fail(ULP_EINVAL, "chunk_bytes must be a positive multiple of 16");
     if (!aligned16(send) || !aligned16(recv)) return fail(ULP_EALIGN, "send/recv must be 16-byte aligned");
-    cudaStream_t st = (cudaStream_t)stream;
-    const size_t P = (size_t)world_size;
-    // recv[p][s] = send[s][p]: for each source s, a 2-D copy of P chunks
-    // (source pitch chunk_bytes, destination pitch P*chunk_bytes).
-    for (size_t s = 0; s < P; ++s) {
-        cudaError_t e = cudaMemcpy2DAsync(recv + s * chunk_bytes, P * chunk_bytes,
-                                          send + s * P * chunk_bytes, chunk_bytes, chunk_bytes, P,
-                                          cudaMemcpyDeviceToDevice, st);
-        if (e != cudaSuccess) return fail(ULP_ECUDA, "alltoall copy: %s", cudaGetErrorString(e));
-    }
-    return ULP_OK;
+    if (send == recv) return fail(ULP_EINVAL, "alltoall: send and recv must not be the same buffer");
+    const size_t vecs = chunk_bytes / 16;
+    const int P = world_size;
+    const size_t per_block = (size_t)kA2AThreads * kA2AVecs;   // 16 KB per block and pass
+    const unsigned gx = (unsigned)std::min<size_t>(65535, (vecs + per_block - 1) / per_block);
+    alltoall_kernel<<<dim3(gx, (unsigned)(P * P)), kA2AThreads, 0, (cudaStream_t)stream>>>(
+        reinterpret_cast<const uint4 *>(send), reinterpret_cast<uint4 *>(recv), P, vecs);
+    return check_launch("alltoall_emulate");
 }
 
 }  // extern "C"

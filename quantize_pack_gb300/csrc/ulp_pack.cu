@@ -46,7 +46,7 @@ struct Slab {
 // tb = 128 g + R hs.  FULL = all of them belong to the rank and none is
 // excluded from the K amax (so no per-row predicate is needed).  GQ = Q group
 // rows: 128 (the slab's group, slot js) or 64 (the K groups).
-template <int D, int DT, int GQ, bool FULL>
+template <int D, int DT, int GQ, bool FOLD, bool FULL>
 __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, int half, PackSmem<D, GQ> &sm)
 {
     constexpr int R = pack_rows<D, GQ>();     // rows of the CTA
@@ -168,17 +168,18 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, int
     const size_t amax_row = (((size_t)sl.rk * a.B + sl.b) * a.H + sl.hh) * a.nk;
     if (warp == 0) {
         // the rank's first/last K groups in this CTA, derived from the
-        // gathered raw-K min/max when they are given (all 32 lanes)
-        float kder[2] = {0.0f, 0.0f};
-        if (a.gathered) {
+        // gathered raw-K min/max when they are given (all 32 lanes; the
+        // value goes to k_amax, where the K scale below reads it)
+        if (FOLD) {
 #pragma unroll
             for (int hk = 0; hk < KG; ++hk) {
                 const int gk = 2 * g + KG * hs + hk;
                 if (gk >= sl.fk && gk <= sl.lk && (gk == sl.fk || gk == sl.lk)) {
-                    kder[hk] = derive_slot_warp<D, DT>(a.gathered, a.k_mean, a.B, a.H, L, a.P, sl.b, sl.hh, gk);
-                    if (lane == 0) a.k_amax[amax_row + (gk - sl.fk)] = kder[hk];
+                    const float d = derive_slot_warp<D, DT>(a.gathered, a.k_mean, a.B, a.H, L, a.P, sl.b, sl.hh, gk);
+                    if (lane == 0) a.k_amax[amax_row + (gk - sl.fk)] = d;
                 }
             }
+            __syncwarp();
         }
         qmax0 = lane < NW ? sm.red[lane][0] : -INFINITY;
         qmax1 = lane < NW ? sm.red[lane][1] : -INFINITY;
@@ -215,9 +216,7 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, int
             if (gk >= sl.fk && gk <= sl.lk) {
                 const int jk = gk - sl.fk;
                 float kam;
-                if ((jk == 0 || jk == sl.tk - 1) && a.gathered) {
-                    kam = kder[hk];
-                } else if (jk == 0 || jk == sl.tk - 1 || !a.fused) {
+                if (jk == 0 || jk == sl.tk - 1 || !a.fused) {
                     kam = a.k_amax[amax_row + jk];
                 } else {
                     kam = floor_eps(hk == 0 ? kmax0 : kmax1);
@@ -344,7 +343,7 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, int
 //     per-warp, then warp 0 merges the warps, applies the boundary rules and
 //     publishes the scales;
 //  4. Q/K codes from the registers; 5. V codes from shared memory.
-template <int D, int DT, int GQ>
+template <int D, int DT, int GQ, bool FOLD>
 __global__ void __launch_bounds__(pack_threads<D, GQ>(), 1024 / pack_threads<D, GQ>()) pack_kernel(PackArgs a)
 {
     constexpr int R = pack_rows<D, GQ>();
@@ -381,14 +380,17 @@ __global__ void __launch_bounds__(pack_threads<D, GQ>(), 1024 / pack_threads<D, 
         const int tb = sl.g * kSlab + hs * R;
         full = tb >= sl.row0 && tb + R <= sl.row0 + a.L && sl.gu != 2 * sl.g + hs;
     }
-    if (full) pack_slab<D, DT, GQ, true>(a, sl, hs, sm);
-    else pack_slab<D, DT, GQ, false>(a, sl, hs, sm);
+    if (full) pack_slab<D, DT, GQ, FOLD, true>(a, sl, hs, sm);
+    else pack_slab<D, DT, GQ, FOLD, false>(a, sl, hs, sm);
 }
 
 template <int D, int DT, int GQ>
 static cudaError_t pack_launch(dim3 grid, cudaStream_t st, bool pdl, const PackArgs &a)
 {
-    return launch_kernel(pack_kernel<D, DT, GQ>, grid, dim3(pack_threads<D, GQ>()), st, pdl, a);
+    // the derive is a separate instantiation: its warp-0 code would otherwise
+    // cost the common kernel registers
+    if (a.gathered) return launch_kernel(pack_kernel<D, DT, GQ, true>, grid, dim3(pack_threads<D, GQ>()), st, pdl, a);
+    return launch_kernel(pack_kernel<D, DT, GQ, false>, grid, dim3(pack_threads<D, GQ>()), st, pdl, a);
 }
 
 }  // namespace ulp

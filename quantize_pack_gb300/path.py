@@ -8,11 +8,12 @@ CUDA graph.
 All P shards sit in device memory; the stats all-gather is the stacked
 [P, ...] buffer the boundary kernel writes, and the all-to-all is folded into
 the pack's store addresses (dest-major send buffer = every destination's
-recv_u8) or, on request, run as a separate device copy.  One step is three
-launches of the CUDA library: boundary min/max -> pack (which derives the K
-boundary slots from the gathered min/max itself) -> unpack; plus derive when
-``fold_derive`` is off, k_grouped_amax when the unfused pack is chosen, and
-the copy when the exchange is not folded.
+recv_u8) or, on request, run as a separate device copy.  One step is four
+launches of the CUDA library: boundary min/max -> derive -> pack -> unpack; or
+three when pack derives the K boundary slots from the gathered min/max itself
+(``fold_derive``, the default for launch-bound workloads); plus
+k_grouped_amax when the unfused pack is chosen, and the copy when the exchange
+is not folded.
 """
 from __future__ import annotations
 
@@ -23,11 +24,14 @@ import torch
 from . import ulp
 
 
+FOLD_BELOW_BYTES = 256 << 20
+
+
 class UlyssesLowpPath:
     def __init__(self, *, B: int, L: int, H: int, D: int, world_size: int, dtype: torch.dtype,
                  used_sequence: Optional[int] = None, scale_sequence: Optional[int] = None,
                  aligned: Optional[bool] = None, q_group: int = ulp.GQ, fused: bool = True,
-                 fold_exchange: bool = True, fold_derive: bool = True,
+                 fold_exchange: bool = True, fold_derive: Optional[bool] = None,
                  pdl: Optional[bool] = None, pdl_unpack: Optional[bool] = None, device="cuda"):
         P = world_size
         self.B, self.L, self.H, self.D, self.P = B, L, H, D, P
@@ -40,7 +44,11 @@ class UlyssesLowpPath:
         self.q_group = q_group
         self.fused = fused
         self.fold_exchange = fold_exchange
-        self.fold_derive = fold_derive
+        # fold_derive: pack derives the K boundary slots itself (one launch
+        # fewer; its warp-0 derive costs the large workloads more than the
+        # launch it saves).  None: fold when the step is launch-bound, i.e.
+        # its Q, K, V inputs are under twice the 129 MB L2.
+        self.fold_derive = (6 * P * B * L * H * D < FOLD_BELOW_BYTES) if fold_derive is None else fold_derive
         # pdl: programmatic launch of pack, which follows the boundary min/max
         # (or derive); neither writes pack's inputs, so pack loads them before
         # waiting;
@@ -62,11 +70,7 @@ class UlyssesLowpPath:
 
     @property
     def launches_per_step(self) -> int:
-        return 3 + (0 if self.fold_derive else 1) + (0 if self.fused else 1)
-
-    @property
-    def copies_per_step(self) -> int:
-        return 0 if self.fold_exchange else P_copies(self.P)
+        return 3 + (0 if self.fold_derive else 1) + (0 if self.fused else 1) + (0 if self.fold_exchange else 1)
 
     def run(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, k_mean: torch.Tensor,
             v_scale: torch.Tensor, on_pack=None, out=None):
@@ -176,8 +180,3 @@ class UlyssesLowpPath:
         with torch.cuda.graph(graph):
             self.run(q, k, v, k_mean, v_scale)
         return graph
-
-
-def P_copies(P: int) -> int:
-    """Copies the emulated all-to-all issues (one 2-D copy per source)."""
-    return P

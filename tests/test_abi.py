@@ -129,3 +129,5 @@ def test_pack_and_derive_reject(lib):
     assert lib.ulp_boundary_minmax(FAKE, FAKE, 0, 1, 96, 8, 64, 0, 2, 500, 128, FAKE, FAKE, None) == -1
     assert lib.ulp_boundary_minmax(FAKE, FAKE, 0, 1, 96, 8, 64, 0, 2, -1, 0, FAKE, FAKE, None) == -1
     assert lib.ulp_alltoall_emulate(FAKE, FAKE, 2, 24, None) == -1
+    assert lib.ulp_alltoall_emulate(FAKE, FAKE, 2, 32, None) == -1      # send == recv
+    assert b"same buffer" in lib.ulp_last_error()

@@ -126,15 +126,21 @@ def test_alltoall_and_unpack(wl):
             gh.assert_bits_equal(one[i], res["out"][p][i], f"{name} dest {p}")
 
 
-@pytest.mark.parametrize("mode", ["fused_folded", "unfused_copy"])
+@pytest.mark.parametrize("mode", ["fused_folded", "unfused_copy", "fused_separate_derive"])
 @pytest.mark.parametrize("wl", GPU_WORKLOADS, ids=lambda w: w.name)
 def test_whole_path(wl, mode):
+    """The step through UlyssesLowpPath: fused pack with the exchange and the
+    derive folded in (three launches); the unfused pack, the derive folded,
+    with the all-to-all as its own copy; the fused pack after a separate
+    derive launch."""
     inp, res, (q, k, v, km, vs) = _setup(wl)
     path = UlyssesLowpPath(B=wl.B, L=wl.L, H=wl.H, D=wl.D, world_size=wl.P,
                            dtype=gh.torch_dtype(wl.dtype), used_sequence=wl.used_sequence,
                            scale_sequence=wl.scale_sequence, aligned=wl.aligned,
-                           q_group=wl.q_group, fused=(mode == "fused_folded"),
-                           fold_exchange=(mode == "fused_folded"))
+                           q_group=wl.q_group, fused=(mode != "unfused_copy"),
+                           fold_exchange=(mode != "unfused_copy"),
+                           fold_derive=(mode != "fused_separate_derive"))
+    assert path.launches_per_step == {"fused_folded": 3, "unfused_copy": 5, "fused_separate_derive": 4}[mode]
     for _ in range(2):                      # a second step on the same buffers
         outs = path.run(q, k, v, km, vs)
         torch.cuda.synchronize()
