@@ -21,8 +21,11 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Every tensor pointer is a DEVICE pointer the caller owns; the library
- *    allocates nothing and keeps no state across calls except a thread-local
- *    last-error string.  Tensors are dense, row-major (C order).  Q, K, V,
+ *    allocates nothing.  Across calls it keeps a thread-local last-error
+ *    string, per-device lookups (launch occupancy, function attributes, the
+ *    driver entry points it uses) and, for ulp_k_mean_global_noalloc, one
+ *    fixed device array with its per-device address (see that entry point).
+ *    Tensors are dense, row-major (C order).  Q, K, V,
  *    k_mean, v_scale, the chunk buffers and q8/k8/v8 must be 16-byte aligned;
  *    the other fp32 buffers (amax, min/max, partials, scales) 4-byte aligned.
  *  - `dtype` is ULP_BF16 or ULP_FP16 for Q/K/V/k_mean.
@@ -171,8 +174,11 @@ int ulp_k_mean_global_grouped(const void *k, int dtype, int B, int L, int H, int
  *     bytes) are rejected with ULP_EINVAL and a message; nothing is launched.
  *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
  *   - The first call on a device looks the array's device address up
- *     (cudaGetSymbolAddress, that device current) and caches it; make that first
- *     call before any stream capture on the device.
+ *     (cudaGetSymbolAddress, that device current) and caches it with the
+ *     context it belongs to; make that first call before any stream capture
+ *     on the device.  After a device reset (a new context, the module loaded
+ *     again) the next call looks the address up again, and that call too
+ *     should come before any capture.
  *   - Every call uses the same array and leaves its nodes there; each call
  *     writes every node it reads, so no clearing is needed.  Calls whose
  *     kernels can overlap on the GPU (other streams, other host threads) race

@@ -256,6 +256,8 @@ int kmean_launch(const void *k, int dtype, int B, int L, int H, int D, int world
     const dim3 grid_a((unsigned)gx, (unsigned)a.ngrp, (unsigned)(world_size * B));
     const long long nb = ((long long)B * H * D + 31) / 32;
     if (nb > INT_MAX) return fail(ULP_EINVAL, "k_mean_global: grid too large");
+    // (kernel B as a programmatic dependent launch was slower: its CTAs,
+    // resident early and waiting, took occupancy from kernel A)
     if (dtype == ULP_BF16) {
         launch_blocks<ULP_BF16>(G, grid_a, stream, a);
         launch_kernel(kmean_finish_kernel<ULP_BF16>, dim3((unsigned)nb), dim3(32 * world_size), stream, false, a);
@@ -333,10 +335,31 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;   // 8 MiB of tree nodes
 static __device__ __align__(256) unsigned char g_kmean_scratch[kNoAllocScratchBytes];
 
-// Device address of g_kmean_scratch per device.  Host code must not use the
-// array's name as an address: on the host it only stands in for the symbol.
+// Device address of g_kmean_scratch per device, with the context it was
+// looked up in.  Host code must not use the array's name as an address: on
+// the host it only stands in for the symbol.  A device reset destroys the
+// context and the module with it; the next call finds another current
+// context and looks the address up again.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
 std::mutex g_scratch_mutex;
 void *g_scratch_addr[128];
+CUcontext g_scratch_ctx[128];
+
+CUcontext current_context()
+{
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
 
 int scratch_address(void **out)
 {
@@ -344,13 +367,15 @@ int scratch_address(void **out)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return ulp::fail(ULP_ECUDA, "k_mean_global_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= 128) return ulp::fail(ULP_EINVAL, "k_mean_global_noalloc: device %d out of range", dev);
+    const CUcontext ctx = current_context();
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || !ctx || g_scratch_ctx[dev] != ctx) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_kmean_scratch);    // with `dev` current
+        e = cudaGetSymbolAddress(&p, g_kmean_scratch);    // with `dev` current (sets its context up if need be)
         if (e != cudaSuccess || !p)
             return ulp::fail(ULP_ECUDA, "k_mean_global_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = current_context();
     }
     *out = g_scratch_addr[dev];
     return ULP_OK;

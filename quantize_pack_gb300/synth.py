@@ -174,3 +174,56 @@ def attention_operands(seed: int, *, B: int, S: int, h: int, D: int, n: Optional
     k8[:, n:] = -127
     v8[..., n:S] = 0x7E
     return AttentionOperands(q8, k8, v8, qs, ks, vs, n, q_group)
+
+
+def attention_operands_paired(seed: int, *, S: int, h: int, D: int, n: int, q_group: int = 128,
+                              logit: float = 40.0) -> AttentionOperands:
+    """Structured, peaky operands for one batch (B = 1): every query tile i
+    (128 rows) has two dominant keys with identical codes, one in key tile
+    i and one in key tile i + 1 (mod the tile count), so its softmax splits
+    its weight about evenly between two values; a key tile that is dropped
+    or counted twice moves those rows by a large fraction of max |V|.
+
+    PCG64 ``default_rng(seed)``, draws in this order: one sign pattern
+    p_i in {-127, 127}^D per query tile and head; Q rows = p_i plus integer
+    noise in [-8, 8] (clipped to [-127, 127]); K codes uniform in [-24, 24];
+    the dominant keys' places (uniform in the first half of a key tile's live
+    rows for its own query tile, in the second half for the previous one); V
+    bytes uniform over the finite E4M3 codes.  Q and K scales are one constant each, chosen so the
+    dominant logits are about ``logit`` (natural units, 1/sqrt(D) softmax
+    scale); V scales uniform in [0.01, 0.05].  Rows past n are set as in
+    attention_operands."""
+    rng = np.random.default_rng(seed)
+    T = (n + 127) // 128                                   # tiles over the live prefix
+    Spad = (S + 63) // 64 * 64
+    pat = np.where(rng.integers(0, 2, size=(T, h, D)) == 1, 127, -127).astype(np.int32)
+    q = np.repeat(pat, 128, axis=0)[:S]
+    if q.shape[0] < S:
+        q = np.concatenate([q, np.zeros((S - q.shape[0], h, D), np.int32)])
+    q = np.clip(q + rng.integers(-8, 9, size=(S, h, D)), -127, 127)
+    k = rng.integers(-24, 25, size=(S, h, D)).astype(np.int32)
+    # key tile t holds query tile t's key in its first half and query tile
+    # t - 1's in its second half (of its live rows), so no two collide
+    u = rng.uniform(0.0, 1.0, size=(T, 2))
+    for i in range(T):
+        for which, t in ((0, i), (1, (i + 1) % T)):
+            r = min(128, n - 128 * t)
+            half = r // 2
+            off = int(u[i, which] * half) if which == 0 else half + int(u[i, which] * (r - half))
+            k[t * 128 + off] = pat[i]
+    v8 = rng.integers(0, 256, size=(1, D, h, Spad)).astype(np.uint8)
+    v8[(v8 & 0x7F) == 0x7F] = 0x3C
+    v8[..., S:] = 0
+    wq, wk = (n + q_group - 1) // q_group, (n + 63) // 64
+    # logit = qs * ks * (127^2 D) / sqrt(D) for a dominant key
+    qk = logit * np.sqrt(D) / (127.0 * 127.0 * D)
+    qs = np.full((1, h, wq), np.sqrt(qk), np.float32)
+    ks = np.full((1, h, wk), np.float32(qk) / qs[0, 0, 0], np.float32)
+    vs = rng.uniform(0.01, 0.05, size=(1, h, D)).astype(np.float32)
+    q8 = q.astype(np.int8)[None]
+    k8 = k.astype(np.int8)[None]
+    q8[:, n:] = 127
+    k8[:, n:] = -127
+    v8[..., n:S] = 0x7E
+    return AttentionOperands(np.ascontiguousarray(q8), np.ascontiguousarray(k8), v8, qs, ks, vs, n, q_group)
+

@@ -1,30 +1,8 @@
 """GPU parity of the attention consumer (ulp_sage_attention) against the fp64
-oracle (oracle/attention.py) on the same seeded operands.
-
-Tolerance, from the kernel's arithmetic (per output element, relative to
-Vmax = max over the live keys of |V[u, d]| for that batch, head and channel):
-  * the integer logits q8 . k8 are exact (fp16 operands, fp32 accumulation of
-    at most 128 products of magnitude <= 2^14);
-  * the weight exponent fma(S, c, -m) with c = fl(fl(q_scale * fl(sm_scale *
-    log2 e)) * k_scale): three roundings in c (3 2^-24 |x|) and one in the
-    fma (2^-24 |x - m| <= 2^-23 xmax, xmax = the largest |x|); the error of m
-    itself shifts every weight alike and cancels.  So each weight 2^(x - m)
-    is off by at most ln2 * 6 * 2^-24 * xmax relative, plus the 2^-22 of the
-    hardware exp2;
-  * so the computed weights' mean is within 2 eps_e Vmax of the exact one,
-    eps_e = 6 ln2 2^-24 xmax + 2^-22;
-  * the numerator's weights are rounded to fp16 (2^-11 relative in the
-    normal range, 2^-25 absolute below it) while the denominator sums the
-    fp32 weights: at most 2^-11 Vmax more, plus n 2^-25 Vmax for the
-    subnormal weights (the largest weight of a row is >= 1, so the sum is);
-    with eps_w = 2^-11 + eps_e, 2 eps_e + 2^-11 <= 2 eps_w;
-  * fp32 accumulation of the n products in the PV MMAs and the O rescales
-    (numerator), and of the row's weights in eight partial sums per tile and
-    one running sum across tiles (denominator): <= 2 (n + ntiles) 2^-23
-    Vmax together; the final scaling by 1/l and v_scale: 3 2^-24.
-bound(n, xmax) = 2 eps_w + n (2^-22 + 2^-25) + (2 ceil(n/128) + 3) 2^-23.
-bf16 / fp16 outputs add one rounding of the result (2^-9 / 2^-12 relative).
-"""
+oracle (oracle/attention.py) on the same seeded operands, within the
+tolerances of attention_check.py (the derived worst case everywhere; also the
+typical bound at full size).  Each test prints its observed max error over
+the worst-case tolerance (pytest -s shows it)."""
 import math
 
 import numpy as np
@@ -33,27 +11,11 @@ import torch
 
 from oracle import attention as A
 from quantize_pack_gb300 import synth, ulp
+import attention_check as ac
 import helpers as hp
 import gpu_helpers as gh
 
 pytestmark = pytest.mark.gpu
-
-
-def bound(n: int, xmax: float) -> float:
-    eps_w = 2.0 ** -11 + 6 * math.log(2) * 2.0 ** -24 * xmax + 2.0 ** -22
-    return 2 * eps_w + n * (2.0 ** -22 + 2.0 ** -25) + (2 * math.ceil(n / 128) + 3) * 2.0 ** -23
-
-
-def extent(c, sm_scale=None):
-    """(Vmax [B, 1, h, D] = max over the live keys of |V|, xmax = the largest
-    |logit| in log2 units)."""
-    Q, K, V = A.dequantize(c.q8, c.k8, c.v8, c.q_scale, c.k_scale, c.v_scale, n=c.n,
-                           q_group=c.q_group)
-    D = c.q8.shape[3]
-    sm = D ** -0.5 if sm_scale is None else sm_scale
-    xmax = max(float(np.abs(Q[b, :, j] @ K[b, :, j].T).max())
-               for b in range(Q.shape[0]) for j in range(Q.shape[2])) * sm / math.log(2)
-    return np.abs(V).max(axis=1, keepdims=True), xmax
 
 
 def run_gpu(c, out_dtype=torch.float32, sm_scale=None):
@@ -72,15 +34,10 @@ def oracle(c, **kw):
                             q_group=c.q_group, **kw)
 
 
-def check(got, want, c, rel_out=0.0, sm_scale=None):
-    vm, xmax = extent(c, sm_scale)
-    tol = bound(c.n, xmax) * vm + rel_out * np.abs(want)
-    err = np.abs(got - want)
-    ratio = np.divide(err, tol, out=np.where(err > 0, np.inf, 0.0), where=tol > 0)
-    worst = np.unravel_index(np.argmax(ratio), err.shape)
-    assert np.all(err <= tol), (f"max err/tol {float(ratio[worst]):.3f} at {worst}: "
-                                f"got {got[worst]} want {want[worst]}")
-    return float(ratio.max())
+def check(got, want, c, **kw):
+    r = ac.check(got, want, c, **kw)
+    print(f"max err / worst-case tolerance: {r:.4f}")
+    return r
 
 
 CASES = [
@@ -103,6 +60,13 @@ def test_attention_matches_oracle(B, S, h, D, n, q_group, spread):
     got = run_gpu(c)
     assert got.shape == (B, n, h, D)
     check(got, oracle(c), c)
+
+
+def test_paired_dominant_keys_within_the_typical_bound():
+    """Structured peaky operands (every query tile's weight split between two
+    equal dominant keys in neighbouring key tiles), ragged live prefix."""
+    c = synth.attention_operands_paired(44, S=1100, h=2, D=128, n=1000)
+    check(run_gpu(c), oracle(c), c, use_typical=True)
 
 
 def test_explicit_softmax_scale():
@@ -172,6 +136,38 @@ def test_full_size_sampled_rows():
         Q, K, V = A.dequantize(cj.q8, cj.k8, cj.v8, cj.q_scale, cj.k_scale, cj.v_scale, n=n,
                                q_group=128)
         xmax = float(np.abs(Q[0, rows, 0] @ K[0, :, 0].T).max()) * D ** -0.5 / math.log(2)
-        tol = bound(n, xmax) * np.abs(V[0, :, 0]).max(axis=0)              # [D]
+        vmax = np.abs(V[0, :, 0]).max(axis=0)                               # [D]
         err = np.abs(got[0, rows, j] - want)
-        assert np.all(err <= tol), (j, float((err / tol).max()))
+        assert np.all(err <= ac.worst(n, xmax) * vmax), (j, float((err / (ac.worst(n, xmax) * vmax)).max()))
+        assert np.all(err <= ac.typical(n, xmax) * vmax), (j, float((err / (ac.typical(n, xmax) * vmax)).max()))
+        print(f"head {j}: max err / worst-case tolerance {float((err / (ac.worst(n, xmax) * vmax)).max()):.4f}")
+
+
+def test_full_size_every_row_paired_keys():
+    """The bench's consumer shape (B=1, S = 8 x 9360, h = 5, D = 128, live
+    prefix 74800) on structured operands: every query tile's softmax splits
+    between two equal dominant keys, one in its own key tile and one in the
+    next (synth.attention_operands_paired), so a key tile dropped or counted
+    twice moves whole rows by a large part of max |V|.  Every query row of
+    head 0 against the oracle (in chunks), within the typical bound, and the
+    observed error at most a tenth of the worst-case tolerance."""
+    S, n, h, D = 8 * 9360, 74800, 5, 128
+    c = synth.attention_operands_paired(43, S=S, h=h, D=D, n=n)
+    got = run_gpu(c, out_dtype=torch.float32)
+    j = 0
+    cj = synth.AttentionOperands(
+        np.ascontiguousarray(c.q8[:, :, j:j + 1]), np.ascontiguousarray(c.k8[:, :, j:j + 1]),
+        np.ascontiguousarray(c.v8[:, :, j:j + 1]), np.ascontiguousarray(c.q_scale[:, j:j + 1]),
+        np.ascontiguousarray(c.k_scale[:, j:j + 1]), np.ascontiguousarray(c.v_scale[:, j:j + 1]),
+        n, 128)
+    want = np.empty((n, D))
+    for r0 in range(0, n, 2048):
+        rows = np.arange(r0, min(r0 + 2048, n))
+        want[rows] = A.sage_attention(cj.q8, cj.k8, cj.v8, cj.q_scale, cj.k_scale, cj.v_scale, n=n,
+                                      q_group=128, rows=rows)[0, :, 0]
+    Q, K, V = A.dequantize(cj.q8, cj.k8, cj.v8, cj.q_scale, cj.k_scale, cj.v_scale, n=n, q_group=128)
+    xmax = max(float(np.abs(Q[0, r0:r0 + 2048, 0] @ K[0, :, 0].T).max()) for r0 in range(0, n, 2048))
+    xmax *= D ** -0.5 / math.log(2)
+    vm = np.abs(V).max(axis=1, keepdims=True)
+    r = check(got[:, :, j:j + 1], want[None, :, None, :], cj, use_typical=True, vm_xmax=(vm, xmax))
+    assert r <= 0.1, f"observed max err is {r:.3f} of the worst-case tolerance (expected <= 0.1)"

@@ -216,3 +216,21 @@ def test_checks_reject_mutant(name):
     class M:
         sage_attention = staticmethod(ns["sage_attention"])
     assert not _checks_pass(M), f"the checks did not catch: {name}"
+
+
+@pytest.mark.parametrize("mode", ["drop", "double"])
+def test_tolerance_rejects_a_key_tile_dropped_or_counted_twice(mode):
+    """The GPU tests' tolerance (attention_check.check, worst case and
+    typical) accepts the oracle's own result on structured operands and
+    rejects the result of a kernel that drops one key tile or counts it twice
+    (that result computed here in float64 by attention_check.perturbed)."""
+    import attention_check as ac
+    from quantize_pack_gb300 import synth
+    c = synth.attention_operands_paired(3, S=1100, h=1, D=128, n=1000)
+    want = A.sage_attention(c.q8, c.k8, c.v8, c.q_scale, c.k_scale, c.v_scale, n=c.n)
+    assert ac.check(want, want, c, use_typical=True) == 0.0
+    for tile in (0, 3, 7):                     # first, inner, the ragged last tile
+        bad = ac.perturbed(c, tile, mode)[None, :, None, :]
+        with pytest.raises(AssertionError, match="worst-case"):
+            ac.check(bad, want, c)
+
