@@ -460,16 +460,24 @@ def run_ours(args, wl, rank, world, dist):
         ulp.sage_attention(q8, k8, v8, qsc, ksc, vs0, n=n_att, q_group=wl.q_group,
                            out=att_out, workspace=att_ws, status=att_status)
 
-    for _ in range(2):
-        attend()
-    ta0, ta1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    def attend8():
+        ulp.sage_attention(q8, k8, v8, qsc, ksc, vs0, n=n_att, q_group=wl.q_group,
+                           out=att_out, workspace=att_ws, status=att_status, pv_fp8=True)
+
+    def time_calls(fn, calls):
+        for _ in range(2):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(calls):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / calls
+
     KA = 5
-    ta0.record(stream)
-    for _ in range(KA):
-        attend()
-    ta1.record(stream)
-    torch.cuda.synchronize()
-    att_ms = ta0.elapsed_time(ta1) / KA
+    att_ms = time_calls(attend, KA)
+    att8_ms = time_calls(attend8, KA)
     att_flops = 4.0 * wl.B * wl.h * n_att * n_att * wl.D
 
     # ---- end to end through the public API with host buffers: E steps from
@@ -575,6 +583,15 @@ def run_ours(args, wl, rank, world, dist):
                               f"({wl.h} heads, {n_att} live rows, D={wl.D}) on its unpacked "
                               "INT8/E4M3 tensors, fp16 tensor cores; 4 n^2 D flops per head; "
                               "not in value"},
+        "attention_e4m3_pv": {
+            "ms": att8_ms, "calls": KA, "tflops": att_flops / (att8_ms * 1e-3) / 1e12,
+            "peak": tensor_peak()[0] * 4 / 3,
+            "peak_kind": "mixed: QK^T at the measured fp16 (= bf16) burst rate, PV at twice it "
+                         "(E4M3, kind::f8f6f4): 4/3 of the fp16 peak for 4 n^2 D flops",
+            "frac": att_flops / (att8_ms * 1e-3) / 1e12 / (tensor_peak()[0] * 4 / 3),
+            "status": int(att_status.item()),
+            "note": "the same call with the PV product in E4M3 (P rounded to E4M3, V read from "
+                    "v8 itself); not in value"},
         "clocks": clocks,
     }
     if small:

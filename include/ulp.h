@@ -91,6 +91,9 @@ typedef void *ulp_stream_t; /* a cudaStream_t */
 
 enum { ULP_BF16 = 0, ULP_FP16 = 1, ULP_F32 = 2 /* attention output only */ };
 
+/* Precision of the attention's PV product (ulp_sage_attention). */
+enum { ULP_PV_F16 = 0, ULP_PV_E4M3 = 1 };
+
 enum {
     ULP_OK = 0,
     ULP_EINVAL = -1, /* argument outside its domain, inconsistent shapes, size overflow */
@@ -304,12 +307,20 @@ int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int D, int wor
  *   V[u, d] = e4m3(v8[d, u]) * v_scale[d],
  *   O[b, t, j, :] = sum_u softmax_u(sm_scale * Q[t] . K[u]) V[u]
  * (K centred by the mean attends the same: q . m is one constant per query).
- * Computed on tensor cores with fp16 operands and fp32 accumulation: the
- * integer logits are exact, P is rounded to fp16 (relative 2^-11) for the PV
- * product and the denominator sums the fp32 weights, so rounding P moves the
- * output by at most 2^-11 of max |V|.  A first kernel widens Q, K and V to
- * fp16 in the workspace (at least ulp_sage_attention_workspace_bytes bytes;
- * contents on return unspecified), the second runs the attention from it.
+ * Computed on tensor cores with fp32 accumulation.  QK^T: fp16 operands, so
+ * the integer logits are exact.  PV, by pv_precision:
+ *   ULP_PV_F16:  P rounded to fp16 (relative 2^-11) and V widened to fp16
+ *                (exactly); the denominator sums the fp32 weights, so rounding
+ *                P moves the output by at most 2^-11 of max |V|;
+ *   ULP_PV_E4M3: P rounded to E4M3 (rn; relative 2^-4 for weights >= 2^-6 of
+ *                the running maximum, absolute 2^-10 below) and V read as the
+ *                E4M3 bytes of v8 itself, at twice the tensor-core rate of
+ *                fp16; the denominator still sums the fp32 weights, so the
+ *                output moves by up to the weight-rounding error (a larger
+ *                bound; see the tests).
+ * A first kernel widens Q and K (and V for ULP_PV_F16) to fp16 in the
+ * workspace (at least ulp_sage_attention_workspace_bytes bytes; contents on
+ * return unspecified), the second runs the attention from it.
  *   q8, k8    [B, S, h, D] int8 (rows >= n are not read)
  *   v8        [B, D, h, Spad] E4M3 bytes, Spad = ceil(S/64)*64
  *   q_scale   [B, h, ceil(n/q_group)] fp32; k_scale [B, h, ceil(n/64)] fp32
@@ -325,7 +336,7 @@ int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int D, int wor
 int ulp_sage_attention(const int8_t *q8, const int8_t *k8, const uint8_t *v8, const float *q_scale,
                        const float *k_scale, const float *v_scale, int B, int S, int h, int D, int n,
                        int q_group, float sm_scale, void *workspace, size_t workspace_bytes,
-                       void *out, int out_dtype, int *status, ulp_stream_t stream);
+                       void *out, int out_dtype, int pv_precision, int *status, ulp_stream_t stream);
 
 /* Workspace bytes ulp_sage_attention needs: 6 * B * h * ceil(n/128)*128 * D
  * (Q, K, V in fp16 over the live prefix rounded up to 128 rows). */

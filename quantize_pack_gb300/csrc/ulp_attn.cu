@@ -158,10 +158,10 @@ struct AttnArgs {
     float scale_log2;                      // sm_scale * log2(e)
 };
 
-template <int D>
+template <int D, bool PV8>
 struct AttnLayout {
     static constexpr uint32_t tBytes = kTile * D * 2;         // a Q or K tile: 128 rows x D
-    static constexpr uint32_t vBytes = D * kTile * 2;         // a V tile: D rows x 128 keys
+    static constexpr uint32_t vBytes = D * kTile * (PV8 ? 1 : 2);   // a V tile: D rows x 128 keys
     static constexpr uint32_t q0 = 0;                         // kQTiles Q tiles
     static constexpr uint32_t k0 = q0 + kQTiles * tBytes;     // kKStages K tiles
     static constexpr uint32_t v0 = k0 + kKStages * tBytes;    // kVStages V tiles
@@ -185,12 +185,12 @@ enum : int {
 };
 static_assert(kNumSlots <= 32, "barrier area");
 
-template <int D>
+template <int D, bool PV8>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     sage_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, AttnArgs a)
 {
-    using Lay = AttnLayout<D>;
+    using Lay = AttnLayout<D, PV8>;
     extern __shared__ uint8_t dyn_smem[];
     // 1024-byte aligned base in the shared window (the swizzle is a function
     // of the address)
@@ -276,8 +276,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     break;
                 tc::mbar_expect_tx(v_full + s, Lay::vBytes);
                 uint8_t *vd = sm + Lay::v0 + s * Lay::vBytes;
-                for (int c = 0; c < 2; ++c)
-                    tc::tma_load_3d(vd + c * (D * 128), &tm_v, i * kTile + c * 64, 0, bh, v_full + s);
+                if (PV8) {
+                    // the E4M3 bytes of v8 itself: D rows of 128 keys (128 B,
+                    // one swizzle row); keys >= n lie outside the map: zeros
+                    tc::tma_load_3d(vd, &tm_v, i * kTile, j, b * D, v_full + s);
+                } else {
+                    for (int c = 0; c < 2; ++c)
+                        tc::tma_load_3d(vd + c * (D * 128), &tm_v, i * kTile + c * 64, 0, bh, v_full + s);
+                }
                 last[s] = i;
             }
             if (*abort) {
@@ -290,6 +296,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // Step i (0 <= i <= ntk): for w = A, B: O_w += P_w(i-1) V(i-1) once
         // the warpgroup has written P_w(i-1), then S_w(i) = Q_w K_i^T.
         if (lane == 0) {
+            // (E4M3 A and B are type 0 of kind::f8f6f4, fp16 type 0 of kind::f16:
+            // the PV descriptor's bits are the same for both)
             constexpr uint32_t idS = tc::idesc_f16_f32(kTile, kTile), idO = tc::idesc_f16_f32(kTile, D);
             bool ok = tc::mbar_wait_abortable(q_full, 0, kWaitNs, abort);
             const uint32_t aq = tc::smem_u32(sm + Lay::q0);
@@ -309,13 +317,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int w = 0; w < kQTiles; ++w) {
                     const uint32_t tS = tS0 + w * kTile;
                     if (i >= 1) {
-                        // A = P_w(i-1): fp16 pairs in the first 64 columns of S_w
+                        // A = P_w(i-1): fp16 pairs in the first 64 columns of S_w, or
+                        // E4M3 quadruples in the first 32 (K = 16 or 32 keys a product)
                         if (!(ok = tc::mbar_wait_abortable(p_ready + w, (i - 1) & 1, kWaitNs, abort))) break;
                         tc::fence_after_sync();
+                        if (PV8) {
 #pragma unroll
-                        for (int k = 0; k < kTile / 16; ++k)
-                            tc::mma_f16_ts(tO0 + w * D, tS + k * 8, tc::sw128_desc_k(av, k, D), idO,
-                                           (i > 1 || k > 0) ? 1u : 0u);
+                            for (int k = 0; k < kTile / 32; ++k)
+                                tc::mma_f8_ts(tO0 + w * D, tS + k * 8, tc::sw128_desc_k(av, k, D), idO,
+                                              (i > 1 || k > 0) ? 1u : 0u);
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < kTile / 16; ++k)
+                                tc::mma_f16_ts(tO0 + w * D, tS + k * 8, tc::sw128_desc_k(av, k, D), idO,
+                                               (i > 1 || k > 0) ? 1u : 0u);
+                        }
                     }
                     if (i < ntk) {
                         const uint32_t aqw = aq + w * Lay::tBytes;
@@ -429,14 +445,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 64; ++e) xh[e] = hf * 64 + e < nvalid ? ex2(fmaf(xh[e], c, nm)) : 0.0f;
                 }
+                if (PV8) {
+                    // E4M3 weights (rn, satfinite; they are <= 2^8 < 448), four
+                    // keys a column: S_w columns 16 hf .. 16 hf + 15
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const __half2 hp = __floats2half2_rn(xh[2 * e], xh[2 * e + 1]);
-                    pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
+                    for (int e = 0; e < 16; ++e) pk[e] = e4m3x4(xh[4 * e], xh[4 * e + 1], xh[4 * e + 2], xh[4 * e + 3]);
+                    tc::tmem_st16u(tS + hf * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const __half2 hp = __floats2half2_rn(xh[2 * e], xh[2 * e + 1]);
+                        pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
+                    }
+                    // P of this half's 64 keys over S_w columns 32 hf .. 32 hf + 31;
+                    // the half's weight sum (four packed partial sums) overlaps the store
+                    tc::tmem_st32u(tS + hf * 32, pk);
                 }
-                // P of this half's 64 keys over S_w columns 32 hf .. 32 hf + 31;
-                // the half's weight sum (four packed partial sums) overlaps the store
-                tc::tmem_st32u(tS + hf * 32, pk);
                 uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
                 for (int e = 0; e < 32; ++e) acc[e & 3] = f2add(acc[e & 3], f2pack(xh[2 * e], xh[2 * e + 1]));
@@ -537,6 +561,35 @@ int make_map(CUtensorMap *m, void *base, uint64_t cols, uint64_t rows, uint64_t 
     return ULP_OK;
 }
 
+// v8 [B, D, h, Spad] E4M3 as a 3-D byte map (keys, head, b * D + d) with
+// boxes of 128 keys x 1 head x D channels and the 128-byte swizzle; the key
+// extent is n, so keys past the live prefix read as zeros.
+int make_v8_map(CUtensorMap *m, const uint8_t *v8, int B, int D, int h, int n, int Spad)
+{
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return fail(ULP_ECUDA, "sage_attention: cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[3] = {(cuuint64_t)n, (cuuint64_t)h, (cuuint64_t)B * D};
+    const cuuint64_t strides[2] = {(cuuint64_t)Spad, (cuuint64_t)h * Spad};
+    const cuuint32_t box[3] = {(cuuint32_t)kTile, 1, (cuuint32_t)D};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(v8), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ULP_ECUDA, "sage_attention: tensor map encoding failed (%d)", (int)r);
+    return ULP_OK;
+}
+
+template <int D, bool PV8>
+void launch_attention(dim3 grid, cudaStream_t st, const CUtensorMap &mq, const CUtensorMap &mk,
+                      const CUtensorMap &mv, const AttnArgs &a)
+{
+    // one CTA per SM (it holds all 512 TMEM columns): the request is padded
+    // past half of the SM's shared memory where the layout is smaller
+    const size_t bytes = std::max<size_t>(AttnLayout<D, PV8>::bytes + 1024, 120 * 1024);
+    cudaFuncSetAttribute(sage_attention_kernel<D, PV8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    sage_attention_kernel<D, PV8><<<grid, kAttnThreads, bytes, st>>>(mq, mk, mv, a);
+}
+
 size_t widened_bytes(int B, int h, int D, int n)
 {
     const size_t T = (size_t)(n + kTile - 1) / kTile * kTile;
@@ -560,7 +613,7 @@ extern "C" int ulp_sage_attention_workspace_bytes(int B, int S, int h, int D, in
 extern "C" int ulp_sage_attention(const int8_t *q8, const int8_t *k8, const uint8_t *v8, const float *q_scale,
                                   const float *k_scale, const float *v_scale, int B, int S, int h, int D,
                                   int n, int q_group, float sm_scale, void *workspace, size_t workspace_bytes,
-                                  void *out, int out_dtype, int *status, ulp_stream_t stream)
+                                  void *out, int out_dtype, int pv_precision, int *status, ulp_stream_t stream)
 {
     if (B < 1 || S < 1 || h < 1) return fail(ULP_EINVAL, "sage_attention: B, S, h must be positive");
     if (D != 64 && D != 128) return fail(ULP_EINVAL, "sage_attention: head_dim must be 64 or 128 (got %d)", D);
@@ -569,6 +622,9 @@ extern "C" int ulp_sage_attention(const int8_t *q8, const int8_t *k8, const uint
     if (out_dtype != ULP_F32 && out_dtype != ULP_BF16 && out_dtype != ULP_FP16)
         return fail(ULP_EDTYPE, "sage_attention: out_dtype must be ULP_F32, ULP_BF16 or ULP_FP16 (got %d)",
                     out_dtype);
+    if (pv_precision != ULP_PV_F16 && pv_precision != ULP_PV_E4M3)
+        return fail(ULP_EINVAL, "sage_attention: pv_precision must be ULP_PV_F16 or ULP_PV_E4M3 (got %d)",
+                    pv_precision);
     if (!(sm_scale > 0.0f) || !(sm_scale < INFINITY))
         return fail(ULP_EINVAL, "sage_attention: sm_scale must be positive and finite");
     if ((long long)B * S * h * D > (1ll << 40) || (long long)B * h > 65535)
@@ -585,15 +641,21 @@ extern "C" int ulp_sage_attention(const int8_t *q8, const int8_t *k8, const uint
     const size_t plane = (size_t)B * h * T * D;
     uint16_t *q16 = reinterpret_cast<uint16_t *>(workspace), *k16 = q16 + plane, *v16 = k16 + plane;
 
+    const bool pv8 = pv_precision == ULP_PV_E4M3;
     CUtensorMap mq, mk, mv;
     if (int s = make_map(&mq, q16, D, T, (uint64_t)B * h, kTile)) return s;
     if (int s = make_map(&mk, k16, D, T, (uint64_t)B * h, kTile)) return s;
-    if (int s = make_map(&mv, v16, T, D, (uint64_t)B * h, D)) return s;
+    if (pv8) {
+        if (int s = make_v8_map(&mv, v8, B, D, h, n, Spad)) return s;
+    } else {
+        if (int s = make_map(&mv, v16, T, D, (uint64_t)B * h, D)) return s;
+    }
 
     const cudaStream_t st = (cudaStream_t)stream;
     WidenArgs w{q8, k8, v8, q16, k16, v16, S, h, D, n, T, Spad};
     const long long chunks = (long long)T * D / 16;
-    const dim3 wgrid((unsigned)((chunks + 255) / 256), (unsigned)(B * h), 3);
+    // blockIdx.z: Q, K (and V, unless the PV product reads v8 itself)
+    const dim3 wgrid((unsigned)((chunks + 255) / 256), (unsigned)(B * h), pv8 ? 2 : 3);
     attn_widen_kernel<<<wgrid, 256, 0, st>>>(w);
     if (int s = check_launch("sage_attention (widen)")) return s;
 
@@ -607,16 +669,12 @@ extern "C" int ulp_sage_attention(const int8_t *q8, const int8_t *k8, const uint
     a.scale_log2 = sm_scale * 1.4426950408889634f;
     // a CTA per pair of query tiles; an odd last tile's partner reads zeros
     const dim3 grid((unsigned)((a.ntk + kQTiles - 1) / kQTiles), (unsigned)h, (unsigned)B);
-    // one CTA per SM (it holds all 512 TMEM columns): at D = 64 the request
-    // is padded past half of the SM's shared memory
     if (D == 128) {
-        const size_t bytes = AttnLayout<128>::bytes + 1024;
-        cudaFuncSetAttribute(sage_attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-        sage_attention_kernel<128><<<grid, kAttnThreads, bytes, st>>>(mq, mk, mv, a);
+        if (pv8) launch_attention<128, true>(grid, st, mq, mk, mv, a);
+        else launch_attention<128, false>(grid, st, mq, mk, mv, a);
     } else {
-        const size_t bytes = std::max<size_t>(AttnLayout<64>::bytes + 1024, 120 * 1024);
-        cudaFuncSetAttribute(sage_attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-        sage_attention_kernel<64><<<grid, kAttnThreads, bytes, st>>>(mq, mk, mv, a);
+        if (pv8) launch_attention<64, true>(grid, st, mq, mk, mv, a);
+        else launch_attention<64, false>(grid, st, mq, mk, mv, a);
     }
     return check_launch("sage_attention");
 }

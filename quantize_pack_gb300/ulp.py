@@ -25,6 +25,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libulp.so")
 ULP_BF16, ULP_FP16, ULP_F32 = 0, 1, 2
 ULP_ALL_RANKS = -1
 SEND_SOURCE_MAJOR, SEND_DEST_MAJOR = 0, 1
+PV_F16, PV_E4M3 = 0, 1   # precision of the attention's PV product
 GK, GQ = 64, 128   # K group rows; default Q group rows (q_group=64 selects the other width)
 
 _STATUS = {-1: "EINVAL", -2: "EDTYPE", -3: "EALIGN", -4: "ECUDA"}
@@ -71,7 +72,7 @@ def lib() -> ctypes.CDLL:
         L.ulp_unpack_for_sage.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                                           _I, _I, _P]
         L.ulp_sage_attention.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
-                                         ctypes.c_float, _P, _SZ, _P, _I, _P, _P]
+                                         ctypes.c_float, _P, _SZ, _P, _I, _I, _P, _P]
         L.ulp_sage_attention_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]
         for name in ("ulp_slots", "ulp_scale_widths", "ulp_chunk_bytes", "ulp_chunk_offsets",
                      "ulp_k_mean_workspace_bytes", "ulp_k_mean_global", "ulp_k_mean_global_noalloc",
@@ -381,7 +382,7 @@ def sage_attention(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale
                    q_group: int = GQ, sm_scale: Optional[float] = None,
                    out: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.bfloat16,
                    workspace: Optional[torch.Tensor] = None,
-                   status: Optional[torch.Tensor] = None) -> torch.Tensor:
+                   status: Optional[torch.Tensor] = None, pv_fp8: bool = False) -> torch.Tensor:
     """Softmax attention over the unpacked tensors of one destination.
 
     q8, k8 [B, S, h, D] int8; v8 [B, D, h, Spad] E4M3 bytes (uint8 or
@@ -393,7 +394,9 @@ def sage_attention(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale
     ``workspace``: optional uint8 device buffer of at least
     sage_attention_workspace_bytes(...) bytes (allocated when None).
     ``status``: optional int32 device tensor of one element, set non-zero by
-    the kernel if a tensor-core product does not complete in time."""
+    the kernel if a tensor-core product does not complete in time.
+    ``pv_fp8``: the PV product in E4M3 (P rounded to E4M3, V read from v8
+    as is) instead of fp16."""
     B, S, h, D = q8.shape
     n = S if n is None else int(n)
     if sm_scale is None:
@@ -410,7 +413,8 @@ def sage_attention(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale
     _check(lib().ulp_sage_attention(_ptr(q8), _ptr(k8), _ptr(v8b), _ptr(q_scale), _ptr(k_scale),
                                     _ptr(v_scale), B, S, h, D, n, q_group, float(sm_scale),
                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                    _ptr(out), _OUT_CODES[out.dtype], st, _stream(q8.device)))
+                                    _ptr(out), _OUT_CODES[out.dtype], PV_E4M3 if pv_fp8 else PV_F16, st,
+                                    _stream(q8.device)))
     return out
 
 

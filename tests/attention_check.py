@@ -102,3 +102,38 @@ def perturbed(c, tile: int, mode: str, b: int = 0, j: int = 0) -> np.ndarray:
     keys = slice(128 * tile, min(128 * tile + 128, c.n))
     p[:, keys] *= 0.0 if mode == "drop" else 2.0
     return (p @ V[b, :, j]) / p.sum(axis=1, keepdims=True)
+
+
+def e4m3_pv_tolerance(c, sm_scale=None):
+    """Per-element tolerance [B, n, h, D] of the E4M3 PV product (P rounded to
+    E4M3, V read as E4M3), from the exact weights of every row.
+
+    With w_u = 2^(x_u - x_max) the exact weight of key u relative to the
+    row's maximum, the kernel rounds w_u * 2^(x_max - m) to E4M3, where its
+    running m lies in [x_max - 8, x_max] (weights stay <= 2^8 < 448, no
+    saturation).  E4M3 keeps 3 mantissa bits: a normal value (>= 2^-6) is
+    off by at most 2^-4 of itself; below, by at most min(2^-10, the value)
+    (half the 2^-9 subnormal step, or the value rounded to zero).  In units
+    of w that is
+        e_u = 2^-4 w_u                 if w_u >= 2^-6,
+        e_u = min(2^-10, w_u)          otherwise.
+    The denominator sums the fp32 weights, so the output moves by at most
+    sum_u e_u |V[u, d]| / sum_u w_u, plus the weights' exponent error (2 eps_e
+    Vmax, as in worst()) and the fp32 accumulation terms of worst()."""
+    Q, K, V = A.dequantize(c.q8, c.k8, c.v8, c.q_scale, c.k_scale, c.v_scale, n=c.n,
+                           q_group=c.q_group)
+    B, n, h, D = Q.shape
+    sm = D ** -0.5 if sm_scale is None else sm_scale
+    tol = np.empty((B, n, h, D))
+    for b in range(B):
+        for j in range(h):
+            x = sm * (Q[b, :, j] @ K[b, :, j].T) / math.log(2)          # log2 units
+            xmax = float(np.abs(x).max())
+            w = np.exp2(x - x.max(axis=1, keepdims=True))
+            e = np.where(w >= 2.0 ** -6, 2.0 ** -4 * w, np.minimum(2.0 ** -10, w))
+            vabs = np.abs(V[b, :, j])
+            eps_e = 6 * math.log(2) * 2.0 ** -24 * xmax + 2.0 ** -22
+            rest = 2 * eps_e + n * 2.0 ** -22 + (2 * math.ceil(n / 128) + 3) * 2.0 ** -23
+            tol[b, :, j] = (e @ vabs) / w.sum(axis=1, keepdims=True) + rest * vabs.max(axis=0)
+    return tol
+

@@ -18,12 +18,12 @@ import gpu_helpers as gh
 pytestmark = pytest.mark.gpu
 
 
-def run_gpu(c, out_dtype=torch.float32, sm_scale=None):
+def run_gpu(c, out_dtype=torch.float32, sm_scale=None, pv_fp8=False):
     dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = ulp.sage_attention(dev(c.q8), dev(c.k8), dev(c.v8), dev(c.q_scale), dev(c.k_scale),
                              dev(c.v_scale), n=c.n, q_group=c.q_group, sm_scale=sm_scale,
-                             out_dtype=out_dtype, status=status)
+                             out_dtype=out_dtype, status=status, pv_fp8=pv_fp8)
     torch.cuda.synchronize()
     assert status.item() == 0, f"tensor-core wait timed out (code {status.item()})"
     return out.float().cpu().numpy().astype(np.float64)
@@ -67,6 +67,33 @@ def test_paired_dominant_keys_within_the_typical_bound():
     equal dominant keys in neighbouring key tiles), ragged live prefix."""
     c = synth.attention_operands_paired(44, S=1100, h=2, D=128, n=1000)
     check(run_gpu(c), oracle(c), c, use_typical=True)
+
+
+@pytest.mark.parametrize("B,S,h,D,n,q_group,spread", CASES,
+                         ids=[f"B{c[0]}_S{c[1]}_h{c[2]}_D{c[3]}_n{c[4]}_gq{c[5]}" for c in CASES])
+def test_e4m3_pv_matches_oracle(B, S, h, D, n, q_group, spread):
+    """The E4M3 PV product (P rounded to E4M3, V straight from v8) against the
+    exact fp64 attention, within the per-row bound of the weights' E4M3
+    rounding (attention_check.e4m3_pv_tolerance); values past the live prefix
+    (NaN codes among them) must not reach the output."""
+    c = synth.attention_operands(100 + S + n, B=B, S=S, h=h, D=D, n=n, q_group=q_group,
+                                 spread=spread)
+    c.v8[..., n:] = 0x7F                     # NaN codes past the prefix (zero-filled keys
+    got = run_gpu(c, pv_fp8=True)            # of the last tile must not read them)
+    want = oracle(c)
+    tol = ac.e4m3_pv_tolerance(c)
+    err = np.abs(got - want)
+    r = float(np.divide(err, tol, out=np.zeros_like(err), where=tol > 0).max())
+    print(f"E4M3 PV: max err / its bound {r:.4f}; max err / max|V| "
+          f"{float((err / np.abs(want).max()).max()):.2e}")
+    assert np.all(np.isfinite(got)) and np.all(err <= tol), r
+
+
+def test_e4m3_pv_paired_keys():
+    c = synth.attention_operands_paired(45, S=1100, h=2, D=128, n=1000)
+    got, want = run_gpu(c, pv_fp8=True), oracle(c)
+    err = np.abs(got - want)
+    assert np.all(err <= ac.e4m3_pv_tolerance(c)), float((err / ac.e4m3_pv_tolerance(c)).max())
 
 
 def test_explicit_softmax_scale():

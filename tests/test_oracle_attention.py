@@ -234,3 +234,24 @@ def test_tolerance_rejects_a_key_tile_dropped_or_counted_twice(mode):
         with pytest.raises(AssertionError, match="worst-case"):
             ac.check(bad, want, c)
 
+
+def test_e4m3_pv_tolerance_holds_for_a_simulated_kernel_and_rejects_a_dropped_tile():
+    """attention_check.e4m3_pv_tolerance, the bound of the E4M3 PV product:
+    the attention with every weight (relative to the row max, and to a max
+    8 log2 units above it, the two ends of the kernel's running max) rounded
+    to E4M3 by torch's cast lies inside it; a dropped key tile does not."""
+    import attention_check as ac
+    from quantize_pack_gb300 import synth
+    c = synth.attention_operands(5, B=1, S=600, h=1, D=64, n=520, q_group=64, spread=16.0)
+    Q, K, V = A.dequantize(c.q8, c.k8, c.v8, c.q_scale, c.k_scale, c.v_scale, n=c.n, q_group=64)
+    x = (Q[0, :, 0] @ K[0, :, 0].T) / 8.0 / math.log(2)
+    want = A.sage_attention(c.q8, c.k8, c.v8, c.q_scale, c.k_scale, c.v_scale, n=c.n, q_group=64)
+    tol = ac.e4m3_pv_tolerance(c)
+    for lag in (0.0, 8.0):
+        w = np.exp2(x - x.max(axis=1, keepdims=True) + lag)
+        w8 = torch.from_numpy(w).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+        sim = (w8 @ V[0, :, 0]) / w.sum(axis=1, keepdims=True)
+        assert np.all(np.abs(sim - want[0, :, 0]) <= tol[0, :, 0]), lag
+    bad = ac.perturbed(c, 2, "drop")
+    assert np.any(np.abs(bad - want[0, :, 0]) > tol[0, :, 0])
+
