@@ -48,14 +48,16 @@ class UlyssesLowpPath:
         # fewer; its warp-0 derive costs the large workloads more than the
         # launch it saves).  None: fold when the step is launch-bound, i.e.
         # its Q, K, V inputs are under twice the 129 MB L2.
-        self.fold_derive = (6 * P * B * L * H * D < FOLD_BELOW_BYTES) if fold_derive is None else fold_derive
+        launch_bound = 6 * P * B * L * H * D < FOLD_BELOW_BYTES
+        self.fold_derive = launch_bound if fold_derive is None else fold_derive
         # pdl: programmatic launch of pack, which follows the boundary min/max
         # (or derive); neither writes pack's inputs, so pack loads them before
         # waiting;
-        # pdl_unpack: of unpack (default off: its early CTAs would sit on SMs
-        # through pack's last wave)
+        # pdl_unpack: of unpack.  None: on for launch-bound steps (its launch
+        # overlaps pack's tail, about 3 us a step), off otherwise (its early
+        # CTAs would sit on SMs through pack's last wave)
         self.pdl_pack = 2 if pdl is None or pdl else 0
-        self.pdl = bool(pdl_unpack)
+        self.pdl = launch_bound if pdl_unpack is None else bool(pdl_unpack)
         self.device = torch.device(device)
         self.chunk_bytes = ulp.chunk_bytes(B, L, self.h, D, q_group)
         f32 = dict(dtype=torch.float32, device=self.device)
