@@ -297,33 +297,61 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
     return w;
 }
 
-// Eight E4M3 codes of rn(x[e] / s[e]) given r[e] = rn(1/s[e]), packed
-// little-endian into two words.  A quotient whose first product y overflowed
-// (possible only with extreme caller scales) sends the group to __fdiv_rn.
-__device__ __forceinline__ uint2 e4m3_codes8(const float (&x)[8], const float (&s)[8],
-                                             const float (&r)[8])
+// fp32 values of the two halves of a 16-bit pair word (low half first).
+template <int DT>
+__device__ __forceinline__ float2 pair_f32(uint32_t w)
 {
-    float z[8];
-    float ym = 0.0f;
+    if (DT == ULP_BF16) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+
+// Eight E4M3 codes of rn(x[e] / s[e]) given r[e] = rn(1/s[e]), x[e] element
+// e of the 16-bit vector v (bf16 or fp16), packed little-endian into two
+// words; rn, satfinite.  z = rn(x / s) by Markstein's correction, then:
+//  - the sign: the correction turns the zero quotient of a negative x into +0
+//    (the -0 + +0 of its last step) and never changes the sign of a nonzero
+//    quotient, so OR-ing x's sign bits (bit 7 of each value's high byte,
+//    gathered by one byte permute per four values) into the code bytes gives
+//    the codes of z with x's sign restored;
+//  - the overflow: the first product y overflows (possible only with extreme
+//    caller scales) exactly when some z is NaN (z = fma(e, r, y) with
+//    e = -inf), i.e. when some code byte reads 0x7F or 0xFF; such a group
+//    goes to __fdiv_rn (as does x = NaN, which gives that code either way).
+template <int DT>
+__device__ __forceinline__ uint2 e4m3_codes8(const uint4 &v, const float (&s)[8], const float (&r)[8])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t c[2];
 #pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-        unsigned long long y2;
-        const unsigned long long z2 = f2quot(f2pack(x[e], x[e + 1]), f2pack(r[e], r[e + 1]),
-                                             f2pack(-s[e], -s[e + 1]), y2);
-        float y0, y1;
-        f2unpack(z2, z[e], z[e + 1]);
-        f2unpack(y2, y0, y1);
-        ym = fmaxf(ym, fmaxf(fabsf(y0), fabsf(y1)));
-        // a zero quotient keeps the sign of x (y has it; the correction's
-        // +0 + -0 would not)
-        z[e] = copysignf(z[e], y0);
-        z[e + 1] = copysignf(z[e + 1], y1);
-    }
-    if (!(ym <= 3.4028235e38f)) {
+    for (int hw = 0; hw < 2; ++hw) {
+        float z[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) z[e] = __fdiv_rn(x[e], s[e]);
+        for (int e = 0; e < 2; ++e) {
+            const int wi = 2 * hw + e;                  // elements 2 wi, 2 wi + 1
+            const float2 x = pair_f32<DT>(w[wi]);
+            unsigned long long y2;
+            const unsigned long long z2 = f2quot(f2pack(x.x, x.y), f2pack(r[2 * wi], r[2 * wi + 1]),
+                                                 f2pack(-s[2 * wi], -s[2 * wi + 1]), y2);
+            f2unpack(z2, z[2 * e], z[2 * e + 1]);
+        }
+        const uint32_t sign = __byte_perm(w[2 * hw], w[2 * hw + 1], 0x7531) & 0x80808080u;
+        c[hw] = e4m3x4(z[0], z[1], z[2], z[3]) | sign;
     }
-    return make_uint2(e4m3x4(z[0], z[1], z[2], z[3]), e4m3x4(z[4], z[5], z[6], z[7]));
+    const uint32_t nan = (((c[0] & 0x7F7F7F7Fu) + 0x01010101u) | ((c[1] & 0x7F7F7F7Fu) + 0x01010101u)) & 0x80808080u;
+    if (nan) {
+        float f[8], z[8];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+            const float2 x = pair_f32<DT>(w[wi]);
+            f[2 * wi] = x.x;
+            f[2 * wi + 1] = x.y;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) z[e] = __fdiv_rn(f[e], s[e]);
+        c[0] = e4m3x4(z[0], z[1], z[2], z[3]);
+        c[1] = e4m3x4(z[4], z[5], z[6], z[7]);
+    }
+    return make_uint2(c[0], c[1]);
 }
 
 // ------------------------------------------------- packed 16-bit min / max
@@ -357,12 +385,5 @@ struct Pair16 {
     }
 };
 
-// fp32 values of the two halves of a 16-bit pair word (low half first).
-template <int DT>
-__device__ __forceinline__ float2 pair_f32(uint32_t w)
-{
-    if (DT == ULP_BF16) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
-}
 
 }  // namespace ulp

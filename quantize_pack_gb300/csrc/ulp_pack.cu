@@ -326,9 +326,8 @@ __device__ __forceinline__ void pack_slab(const PackArgs &a, const Slab &sl, int
     for (int i = 0; i < IT; ++i) {
         const int t = t_first + i * RL;
         if (valid(t)) {
-            float f[8];
-            to_f32x8<DT>(sm.vtile[(i * RL + rl) * NV + c], f);
-            *reinterpret_cast<uint2 *>(out_base + (size_t)t * hD + a.lay.v) = e4m3_codes8(f, vs, vr);
+            *reinterpret_cast<uint2 *>(out_base + (size_t)t * hD + a.lay.v) =
+                e4m3_codes8<DT>(sm.vtile[(i * RL + rl) * NV + c], vs, vr);
         }
     }
 }
