@@ -36,7 +36,6 @@ __global__ void __launch_bounds__(kMeanThreads) kmean_blocks_kernel(KMeanArgs a)
 {
     static_assert(G == 1 || G == 2 || G == 4 || G == 8, "blocks per thread");
     constexpr int LV = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;   // in-thread tree levels
-    pdl_trigger();
     pdl_wait();
     const int HD = a.H * a.D;
     const int vec = blockIdx.x * kMeanThreads + threadIdx.x;     // 4-channel vector of the row
@@ -106,6 +105,10 @@ __global__ void __launch_bounds__(kMeanThreads) kmean_blocks_kernel(KMeanArgs a)
     double *dst = a.nodes + (((size_t)r * a.B + b) * a.ngrp + grp) * HD + (size_t)vec * 4;
 #pragma unroll
     for (int x = 0; x < 4; ++x) dst[x] = top[x];
+    // kernel B may launch once every CTA has come this far (or exited): its
+    // CTAs then take no slot from kernel A's later waves, and its launch
+    // overlaps A's last CTAs (it waits for A's completion before reading)
+    pdl_trigger();
 }
 
 // Kernel B: CTAs of 32 * P threads, thread (rank r, lane c) finishes rank r's
@@ -256,14 +259,14 @@ int kmean_launch(const void *k, int dtype, int B, int L, int H, int D, int world
     const dim3 grid_a((unsigned)gx, (unsigned)a.ngrp, (unsigned)(world_size * B));
     const long long nb = ((long long)B * H * D + 31) / 32;
     if (nb > INT_MAX) return fail(ULP_EINVAL, "k_mean_global: grid too large");
-    // (kernel B as a programmatic dependent launch was slower: its CTAs,
-    // resident early and waiting, took occupancy from kernel A)
+    // kernel B is a programmatic dependent launch of kernel A, whose CTAs
+    // allow it only after their work
     if (dtype == ULP_BF16) {
         launch_blocks<ULP_BF16>(G, grid_a, stream, a);
-        launch_kernel(kmean_finish_kernel<ULP_BF16>, dim3((unsigned)nb), dim3(32 * world_size), stream, false, a);
+        launch_kernel(kmean_finish_kernel<ULP_BF16>, dim3((unsigned)nb), dim3(32 * world_size), stream, true, a);
     } else {
         launch_blocks<ULP_FP16>(G, grid_a, stream, a);
-        launch_kernel(kmean_finish_kernel<ULP_FP16>, dim3((unsigned)nb), dim3(32 * world_size), stream, false, a);
+        launch_kernel(kmean_finish_kernel<ULP_FP16>, dim3((unsigned)nb), dim3(32 * world_size), stream, true, a);
     }
     return check_launch("k_mean_global");
 }
