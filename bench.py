@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--derive", choices=["auto", "folded", "separate"], default="auto",
                     help="boundary derive inside pack (three launches) or its own launch (four); "
                          "auto: inside pack for launch-bound workloads")
+    ap.add_argument("--launch", choices=["single", "multi"], default="multi",
+                    help="the step as three or four launches (multi, the default) or as one "
+                         "cooperative launch (single)")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum CPU time spent on the oracle baseline sample")
@@ -348,6 +351,7 @@ def run_ours(args, wl, rank, world, dist):
                            used_sequence=wl.used_sequence, scale_sequence=wl.scale_sequence,
                            aligned=wl.aligned, q_group=wl.q_group, fused=(args.mode == "fused"),
                            fold_exchange=True, fold_derive={"auto": None, "folded": True, "separate": False}[args.derive],
+                           single_launch=args.launch == "single" and args.derive != "separate",
                            device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -523,31 +527,24 @@ def run_ours(args, wl, rank, world, dist):
         timed region (for comparing runs whose clocks differ)."""
         return None if mhz is None else t_ms * 1e-3 * mhz * 1e6
     pack_gbs = metrics.pack_bytes(wl) / (pack_ms * 1e-3) / 1e9
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": vms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {
-            "workload": wl.name, **{k_: v_ for k_, v_ in wl.describe().items() if k_ != "workload"},
-            "path": f"{args.mode} amax+pack (exchange folded into the stores) + unpack, "
-                    f"{path.launches_per_step} launches/step",
-            "l2": (f"value: L2 ({l2_bytes / 1e6:.0f} MB) flushed before each timed step (a {2 * l2_bytes / 1e6:.0f} MB "
-                   f"write, not timed)" if small else f"inputs {6 * wl.N / 1e9:.2f} GB > 129 MB L2; no flush"),
-            "parallelism": f"{world} independent replica(s) of a P={wl.P} emulated Ulysses group",
-        },
-        "tokens_per_s": wl.tokens * world / (vms * 1e-3),
-        "hbm_frac": value / world / peak,
-        "step_bytes": step_bytes,
-        "roofline": {"bound": "hbm", "kernel": "pack_kernel", "achieved": pack_gbs, "peak": peak,
-                     "peak_kind": f"{peak_kind} (STREAM copy)", "unit": "GB/s",
-                     "frac": pack_gbs / peak, "traffic": recorded_traffic(wl.name),
-                     "algorithmic_bytes_per_launch": metrics.pack_bytes(wl),
-                     "launch_ms": pack_ms},
-        "e2e": {"value": whole_job_value(step_bytes, world, e2e_ms), "unit": "GB/s",
-                "ms_per_step": e2e_ms, "steps": E, "runs_ms_per_step": e2e_runs,
-                "timing": "median of 5 timed runs of E pipelined steps (UlyssesLowpPath.run_host)",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "kernels": {
+    if path.single_launch:
+        # one launch a step: the events around it time the whole step, whose
+        # algorithmic bytes are the step's
+        step_gbs = step_bytes / (pack_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "group_step_kernel", "achieved": step_gbs, "peak": peak,
+                    "peak_kind": f"{peak_kind} (STREAM copy)", "unit": "GB/s", "frac": step_gbs / peak,
+                    "traffic": None, "algorithmic_bytes_per_launch": step_bytes, "launch_ms": pack_ms}
+        kernels = {"group_step": {"ms": pack_ms, "gbs": step_gbs, "frac": step_gbs / peak,
+                                  "algorithmic_bytes": step_bytes, "sm_cycles": cycles(pack_ms)}}
+        path_desc = (f"{args.mode} amax+pack (exchange folded into the stores) + unpack, one cooperative "
+                     "launch/step (boundary min/max, pack with the derive folded in, unpack; grid barriers)")
+    else:
+        roofline = {"bound": "hbm", "kernel": "pack_kernel", "achieved": pack_gbs, "peak": peak,
+                    "peak_kind": f"{peak_kind} (STREAM copy)", "unit": "GB/s",
+                    "frac": pack_gbs / peak, "traffic": recorded_traffic(wl.name),
+                    "algorithmic_bytes_per_launch": metrics.pack_bytes(wl),
+                    "launch_ms": pack_ms}
+        kernels = {
             "pack": {"ms": pack_ms, "gbs": pack_gbs, "frac": pack_gbs / peak,
                      "algorithmic_bytes": metrics.pack_bytes(wl), "sm_cycles": cycles(pack_ms)},
             "unpack": {"ms": unpack_ms,
@@ -556,9 +553,31 @@ def run_ours(args, wl, rank, world, dist):
                        "algorithmic_bytes": metrics.unpack_bytes(wl), "sm_cycles": cycles(unpack_ms)},
             "boundary_minmax" + ("" if path.fold_derive else "+derive"): {
                 "ms": max(0.0, ms - pack_ms - unpack_ms), "sm_cycles": cycles(max(0.0, ms - pack_ms - unpack_ms))},
-            "note": "CUDA events around each launch inside the timed steps (means); sm_cycles = "
-                    "ms x the median SM clock sampled in the timed region",
+        }
+        path_desc = (f"{args.mode} amax+pack (exchange folded into the stores) + unpack, "
+                     f"{path.launches_per_step} launches/step")
+    kernels["note"] = ("CUDA events around each launch inside the timed steps (means); sm_cycles = "
+                       "ms x the median SM clock sampled in the timed region")
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": vms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": wl.name, **{k_: v_ for k_, v_ in wl.describe().items() if k_ != "workload"},
+            "path": path_desc,
+            "l2": (f"value: L2 ({l2_bytes / 1e6:.0f} MB) flushed before each timed step (a {2 * l2_bytes / 1e6:.0f} MB "
+                   f"write, not timed)" if small else f"inputs {6 * wl.N / 1e9:.2f} GB > 129 MB L2; no flush"),
+            "parallelism": f"{world} independent replica(s) of a P={wl.P} emulated Ulysses group",
         },
+        "tokens_per_s": wl.tokens * world / (vms * 1e-3),
+        "hbm_frac": value / world / peak,
+        "step_bytes": step_bytes,
+        "roofline": roofline,
+        "e2e": {"value": whole_job_value(step_bytes, world, e2e_ms), "unit": "GB/s",
+                "ms_per_step": e2e_ms, "steps": E, "runs_ms_per_step": e2e_runs,
+                "timing": "median of 5 timed runs of E pipelined steps (UlyssesLowpPath.run_host)",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "kernels": kernels,
         "alltoall_emulate": {"ms": a2a_ms, "calls": KX, "bytes": a2a_bytes,
                              "gbs": a2a_bytes / (a2a_ms * 1e-3) / 1e9,
                              "frac": a2a_bytes / (a2a_ms * 1e-3) / 1e9 / peak, "sm_cycles": cycles(a2a_ms),

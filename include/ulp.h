@@ -17,6 +17,8 @@
  *                               Returns: the V scale stays with the caller)
  *   ulp_alltoall_emulate        the all-to-all of the chunks, as a device-local copy
  *   ulp_unpack_for_sage         page "...unpack_for_sage"
+ *   ulp_group_step              boundary min/max + pack (derive and exchange folded) +
+ *                               unpack of a whole emulated group in one launch
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -296,6 +298,37 @@ int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int D, int wor
                         int aligned, int scale_sequence, int q_group, int8_t *q8, int8_t *k8,
                         uint8_t *v8, float *q_scale, float *k_scale, int num_dests,
                         int enable_pdl, ulp_stream_t stream);
+
+/* One step of an emulated Ulysses group (every rank, every destination) in a
+ * single cooperative launch: ulp_boundary_minmax (ULP_ALL_RANKS), then
+ * ulp_pack with gathered_minmax given (the boundary derive of page
+ * "derive_k_boundary_amax" folded in), fused = 1 and ULP_SEND_DEST_MAJOR
+ * into recv (the all-to-all folded into the stores; page "unpack_for_sage",
+ * recv_u8), then ulp_unpack_for_sage of all P destinations
+ * (num_dests = world_size).  Every output equals, bit for bit, that of
+ * those three calls with the same arguments: minmax [P, B, H, 2, 2, D] and
+ * q_partial [P, B, H, 2] as written by ulp_boundary_minmax, k_amax
+ * [P, B, H, slots(L,64)] as by ulp_pack, recv [P_dst, P_src, chunk_bytes],
+ * and the unpacked q8, k8, v8, q_scale, k_scale with a leading P axis.  It
+ * takes one launch instead of three: it helps where the host's launch rate
+ * bounds the step (small steps called eagerly).  In GPU time the three
+ * launches chained by programmatic launch are faster: each grid barrier
+ * costs about 2 us, and the fused kernel runs one CTA per SM.
+ *   The phases are separated by grid-wide barriers in `barrier`: two 32-bit
+ *   words of device memory (4-byte aligned) that must be zero before the
+ *   first call and that every completed call leaves zero-count again.  Calls
+ *   that may run concurrently (other streams) need their own pair.  Each
+ *   barrier wait is bounded (1 s); on a timeout the kernel writes 2 to
+ *   *status (a device int, or NULL) and returns early with outputs
+ *   undefined, and the pair must be zeroed again before the next call.  A
+ *   cooperative launch needs every CTA resident, so the grid is capped by the
+ *   occupancy of the device; a launch that still cannot be made gives
+ *   ULP_ECUDA. */
+int ulp_group_step(const void *q, const void *k, const void *v, const void *k_mean, int dtype,
+                   const float *v_scale, int B, int L, int H, int D, int world_size, int used_sequence,
+                   int q_group, int aligned, int scale_sequence, float *minmax, float *q_partial,
+                   float *k_amax, uint8_t *recv, int8_t *q8, int8_t *k8, uint8_t *v8, float *q_scale,
+                   float *k_scale, unsigned *barrier, int *status, ulp_stream_t stream);
 
 /* Attention over the unpacked tensors of one destination -- the consumer the
  * page "unpack_for_sage" hands its outputs to (INT8 Q/K, FP8 E4M3 V, FP32

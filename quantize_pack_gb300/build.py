@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(OUT_DIR, "libulp.so")
 OBJ_DIR = os.path.join(ROOT, "_build", "ulp")
 
 SOURCES = ["ulp_host.cu", "ulp_amax.cu", "ulp_pack.cu", "ulp_unpack.cu", "ulp_kmean.cu",
-           "ulp_attn.cu"]
+           "ulp_attn.cu", "ulp_step.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr"]

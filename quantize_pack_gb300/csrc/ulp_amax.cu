@@ -6,7 +6,7 @@
 // Threads own one 16-byte column vector (8 channels) and a row lane; loads are
 // 16-byte and coalesced along the head's D contiguous elements; the maxima are
 // fp32 fmaxf trees (exact, so order-independent).
-#include "ulp_internal.cuh"
+#include "ulp_minmax.cuh"
 
 namespace ulp {
 
@@ -80,111 +80,14 @@ __global__ void __launch_bounds__(128) k_grouped_amax_kernel(AmaxArgs a)
     }
 }
 
-struct MinmaxArgs {
-    const uint16_t *k, *q;
-    float *minmax, *qpart;
-    int B, L, H, P, rank, used;
-    int gq;   // Q group rows, 64 or 128
-};
-
 // One CTA per (rank, b, head, e): e = 0 first touched group, e = 1 last.
 template <int D, int DT>
 __global__ void __launch_bounds__(128) boundary_minmax_kernel(MinmaxArgs a)
 {
-    constexpr int NV = D / 8, RL = 128 / NV, ITK = kGK / RL, ITQ = kGQ / RL;
+    __shared__ MinmaxSmem<D> sm;
     pdl_trigger();
     pdl_wait();
-    int blk = blockIdx.x;
-    const int e = blk & 1; blk >>= 1;
-    const int hh = blk % a.H; blk /= a.H;
-    const int b = blk % a.B; blk /= a.B;
-    const int rk = blk;
-    const int r = a.rank >= 0 ? a.rank : rk;
-    const int row0 = r * a.L;
-    const int c = threadIdx.x % NV, rl = threadIdx.x / NV;
-    const size_t HD = (size_t)a.H * D;
-    const size_t off = (size_t)rk * a.B * a.L * HD + (size_t)b * a.L * HD + (size_t)hh * D + c * 8;
-
-    // ---- K: raw min / max per channel over the live rows of the group
-    const int g = e == 0 ? first_group(r, a.L, kGK) : last_group(r, a.L, kGK);
-    const int lo = max(g * kGK, row0);
-    const int hi = min(min(g * kGK + kGK, row0 + a.L), a.used);
-    float mn[8], mx[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { mn[i] = INFINITY; mx[i] = -INFINITY; }
-    {
-        uint4 v[ITK];
-#pragma unroll
-        for (int i = 0; i < ITK; ++i) {
-            const int t = g * kGK + i * RL + rl;
-            if (t >= lo && t < hi) v[i] = ld_stream(a.k + off + (size_t)(t - row0) * HD);
-        }
-#pragma unroll
-        for (int i = 0; i < ITK; ++i) {
-            const int t = g * kGK + i * RL + rl;
-            if (t >= lo && t < hi) {
-                float f[8];
-                to_f32x8<DT>(v[i], f);
-#pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                    const float y = f[x] == 0.0f ? 0.0f : f[x];   // -0 -> +0
-                    mn[x] = fminf(mn[x], y);
-                    mx[x] = fmaxf(mx[x], y);
-                }
-            }
-        }
-    }
-    __shared__ float smn[RL][D], smx[RL][D];
-#pragma unroll
-    for (int x = 0; x < 8; ++x) {
-        smn[rl][c * 8 + x] = mn[x];
-        smx[rl][c * 8 + x] = mx[x];
-    }
-
-    // ---- Q: partial amax over the rank's rows of its first / last Q group
-    // (ITQ covers the widest group; rows past a narrower group fail the test)
-    const int gq = e == 0 ? first_group(r, a.L, a.gq) : last_group(r, a.L, a.gq);
-    const int qlo = max(gq * a.gq, row0), qhi = min(gq * a.gq + a.gq, row0 + a.L);
-    float qa = -INFINITY;
-    {
-        uint4 v[ITQ];
-#pragma unroll
-        for (int i = 0; i < ITQ; ++i) {
-            const int t = gq * a.gq + i * RL + rl;
-            if (t >= qlo && t < qhi) v[i] = ld_stream(a.q + off + (size_t)(t - row0) * HD);
-        }
-#pragma unroll
-        for (int i = 0; i < ITQ; ++i) {
-            const int t = gq * a.gq + i * RL + rl;
-            if (t >= qlo && t < qhi) {
-                float f[8];
-                to_f32x8<DT>(v[i], f);
-#pragma unroll
-                for (int x = 0; x < 8; ++x) qa = fmaxf(qa, fabsf(f[x]));
-            }
-        }
-    }
-    __shared__ float red[4];
-    qa = warp_max(qa);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = qa;
-    __syncthreads();
-
-    const size_t obase = ((((size_t)rk * a.B + b) * a.H + hh) * 2 + e) * 2 * D;
-    if (threadIdx.x < D) {
-        const int d = threadIdx.x;
-        float vmin = INFINITY, vmax = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < RL; ++i) {
-            vmin = fminf(vmin, smn[i][d]);
-            vmax = fmaxf(vmax, smx[i][d]);
-        }
-        a.minmax[obase + d] = vmin;
-        a.minmax[obase + D + d] = vmax;
-    }
-    if (threadIdx.x == 0) {
-        const float v = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-        a.qpart[(((size_t)rk * a.B + b) * a.H + hh) * 2 + e] = floor_eps(v);
-    }
+    boundary_minmax_unit<D, DT>(a, blockIdx.x, threadIdx.x, sm, SyncCta{});
 }
 
 struct DeriveArgs {

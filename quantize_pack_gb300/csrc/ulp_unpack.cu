@@ -11,156 +11,21 @@
 //    both sides; blocks copy 32 KiB pieces, 16 vectors of 16 bytes in flight
 //    per thread.
 //  - scales: one thread per output slot.
-#include "ulp_internal.cuh"
+#include "ulp_unpack.cuh"
 
 namespace ulp {
-
-constexpr int kUnpackThreads = 128;
-constexpr int kCopyVecPerThread = 16;
-constexpr int kCopyPiece = kUnpackThreads * kCopyVecPerThread * 16;   // bytes per copy block
-
-struct UnpackArgs {
-    const uint8_t *recv;
-    int8_t *q8, *k8;
-    uint8_t *v8;
-    float *qs, *ks;
-    ChunkLayout lay;
-    int B, L, h, P, S, Spad, wq, wk, nq, nk, nd;
-    int gq;                    // Q group rows, 64 or 128
-    int TT, CC;                // V tiles: t-tiles of 128 rows, 64-byte column blocks
-    long long nVtiles, nVblk;  // V warp tiles, V blocks
-    long long pieces, nCblk;   // copy pieces per span, copy blocks
-    long long nSblk;           // scale blocks
-};
-
-__device__ __forceinline__ void transpose4x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                             uint32_t &b0, uint32_t &b1, uint32_t &b2, uint32_t &b3)
-{
-    const uint32_t t0 = __byte_perm(a0, a1, 0x5140), t1 = __byte_perm(a0, a1, 0x7362);
-    const uint32_t t2 = __byte_perm(a2, a3, 0x5140), t3 = __byte_perm(a2, a3, 0x7362);
-    b0 = __byte_perm(t0, t2, 0x5410);
-    b1 = __byte_perm(t0, t2, 0x7632);
-    b2 = __byte_perm(t1, t3, 0x5410);
-    b3 = __byte_perm(t1, t3, 0x7632);
-}
-
-template <int D>
-__device__ __forceinline__ void unpack_v_tile(const UnpackArgs &a, long long tile)
-{
-    const int lane = threadIdx.x & 31;
-    const int tb = lane >> 2, cbk = lane & 3;
-    const int cc = (int)(tile % a.CC); tile /= a.CC;
-    const int tt = (int)(tile % a.TT); tile /= a.TT;
-    const int b = (int)(tile % a.B);
-    const int p = (int)(tile / a.B);
-    const size_t cbytes = a.lay.bytes;
-    const size_t hD = (size_t)a.h * D;
-    const uint8_t *rbase = a.recv + (size_t)p * a.P * cbytes + a.lay.v + (size_t)b * a.L * hD;
-    const int t0 = tt * 128 + tb * 16;
-    const int col = cc * 64 + cbk * 16;
-
-    uint32_t w[16][4];
-    {
-        int s = t0 / a.L, tl = t0 - s * a.L;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (t0 + i < a.S) v = ld_stream(rbase + (size_t)s * cbytes + (size_t)tl * hD + col);
-            w[i][0] = v.x; w[i][1] = v.y; w[i][2] = v.z; w[i][3] = v.w;
-            if (++tl == a.L) { tl = 0; ++s; }
-        }
-    }
-    if (t0 >= a.Spad) return;
-    uint8_t *obase = a.v8 + (size_t)p * a.B * D * a.h * a.Spad + t0;
-#pragma unroll
-    for (int qw = 0; qw < 4; ++qw) {              // 4 source columns per word
-        uint32_t o[4][4];                         // [column in word][row word]
-#pragma unroll
-        for (int pr = 0; pr < 4; ++pr)            // 4 rows per word
-            transpose4x4(w[4 * pr][qw], w[4 * pr + 1][qw], w[4 * pr + 2][qw], w[4 * pr + 3][qw],
-                         o[0][pr], o[1][pr], o[2][pr], o[3][pr]);
-#pragma unroll
-        for (int n = 0; n < 4; ++n) {
-            const int c = col + 4 * qw + n;
-            const int j = c / D, d = c % D;
-            uint8_t *dst = obase + (((size_t)b * D + d) * a.h + j) * a.Spad;
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(o[n][0], o[n][1], o[n][2], o[n][3]);
-        }
-    }
-}
 
 template <int D>
 __global__ void __launch_bounds__(kUnpackThreads) unpack_kernel(UnpackArgs a)
 {
     pdl_trigger();
     pdl_wait();
-    long long blk = blockIdx.x;
-    if (blk < a.nVblk) {
-        const long long tile = blk * (kUnpackThreads / 32) + (threadIdx.x >> 5);
-        if (tile < a.nVtiles) unpack_v_tile<D>(a, tile);
-        return;
-    }
-    blk -= a.nVblk;
-    const size_t cbytes = a.lay.bytes;
-    const size_t hD = (size_t)a.h * D;
-    if (blk < a.nCblk) {
-        // span = (p, tensor, b, s): L*h*D contiguous bytes on both sides
-        long long span = blk / a.pieces;
-        const long long piece = blk % a.pieces;
-        const int s = (int)(span % a.P); span /= a.P;
-        const int b = (int)(span % a.B); span /= a.B;
-        const int tensor = (int)(span % 2);
-        const int p = (int)(span / 2);
-        const size_t len = (size_t)a.L * hD;
-        const uint4 *src = reinterpret_cast<const uint4 *>(
-            a.recv + ((size_t)p * a.P + s) * cbytes + (tensor ? a.lay.k : a.lay.q) + (size_t)b * len);
-        uint4 *dst = reinterpret_cast<uint4 *>(
-            (tensor ? a.k8 : a.q8) + (size_t)p * a.B * a.S * hD + ((size_t)b * a.S + (size_t)s * a.L) * hD);
-        const size_t nvec = len / 16;
-        const size_t v0 = (size_t)piece * (kCopyPiece / 16) + threadIdx.x;
-        uint4 v[kCopyVecPerThread];
-#pragma unroll
-        for (int i = 0; i < kCopyVecPerThread; ++i) {
-            const size_t idx = v0 + (size_t)i * kUnpackThreads;
-            if (idx < nvec) v[i] = ld_stream(src + idx);
-        }
-#pragma unroll
-        for (int i = 0; i < kCopyVecPerThread; ++i) {
-            const size_t idx = v0 + (size_t)i * kUnpackThreads;
-            if (idx < nvec) dst[idx] = v[i];
-        }
-        return;
-    }
-    blk -= a.nCblk;
-    // scales: one thread per output slot
-    const long long per = (long long)a.B * a.h * (a.wq + a.wk);
-    const long long idx = blk * kUnpackThreads + threadIdx.x;
-    if (idx >= per * a.nd) return;
-    const int p = (int)(idx / per);
-    long long rem = idx % per;
-    const int bj = (int)(rem / (a.wq + a.wk));
-    int g = (int)(rem % (a.wq + a.wk));
-    const uint8_t *rp = a.recv + (size_t)p * a.P * cbytes;
-    if (g < a.wq) {
-        const int s = (g * a.gq) / a.L;
-        const float *src = reinterpret_cast<const float *>(rp + (size_t)s * cbytes + a.lay.qs);
-        a.qs[((size_t)p * a.B * a.h + bj) * a.wq + g] = src[(size_t)bj * a.nq + (g - first_group(s, a.L, a.gq))];
-    } else {
-        g -= a.wq;
-        const int s = (g * kGK) / a.L;
-        const float *src = reinterpret_cast<const float *>(rp + (size_t)s * cbytes + a.lay.ks);
-        a.ks[((size_t)p * a.B * a.h + bj) * a.wk + g] = src[(size_t)bj * a.nk + (g - first_group(s, a.L, kGK))];
-    }
+    unpack_unit<D>(a, blockIdx.x, threadIdx.x);
 }
 
-}  // namespace ulp
-
-using namespace ulp;
-
-extern "C" int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int D, int world_size,
-                                   int aligned, int scale_sequence, int q_group, int8_t *q8,
-                                   int8_t *k8, uint8_t *v8, float *q_scale, float *k_scale,
-                                   int num_dests, int enable_pdl, ulp_stream_t stream)
+int unpack_setup(UnpackArgs &a, long long &blocks, const uint8_t *recv, int B, int L, int h, int D,
+                 int world_size, int aligned, int scale_sequence, int q_group, int8_t *q8, int8_t *k8,
+                 uint8_t *v8, float *q_scale, float *k_scale, int num_dests)
 {
     if (int s = check_world(world_size)) return s;
     if (int s = check_q_group(q_group, "unpack")) return s;
@@ -170,7 +35,6 @@ extern "C" int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int
     if (aligned < -1 || aligned > 1) return fail(ULP_EINVAL, "unpack: aligned must be -1, 0 or 1");
     if (aligned == 1 && L % 128 != 0)
         return fail(ULP_EINVAL, "unpack: aligned=True requires local_sequence %% 128 == 0 (L = %d)", L);
-    if (enable_pdl < -1 || enable_pdl > 2) return fail(ULP_EINVAL, "unpack: enable_pdl must be -1, 0, 1 or 2");
     if ((long long)L * world_size > INT_MAX / 2) return fail(ULP_EINVAL, "unpack: sequence too long");
     const int S = L * world_size;
     if (scale_sequence != -1 && (scale_sequence < 1 || scale_sequence > S))
@@ -179,7 +43,7 @@ extern "C" int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int
         !aligned4(k_scale))
         return fail(ULP_EALIGN, "unpack: recv, q8, k8, v8 must be 16-byte aligned, scales 4-byte aligned");
 
-    UnpackArgs a{};
+    a = UnpackArgs{};
     a.recv = recv; a.q8 = q8; a.k8 = k8; a.v8 = v8; a.qs = q_scale; a.ks = k_scale;
     a.lay = chunk_layout(B, L, h, D, q_group);
     a.gq = q_group;
@@ -197,8 +61,26 @@ extern "C" int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int
     a.pieces = ((long long)L * h * D + kCopyPiece - 1) / kCopyPiece;
     a.nCblk = (long long)num_dests * 2 * B * world_size * a.pieces;
     a.nSblk = ((long long)num_dests * B * h * (a.wq + a.wk) + kUnpackThreads - 1) / kUnpackThreads;
-    const long long blocks = a.nVblk + a.nCblk + a.nSblk;
+    blocks = a.nVblk + a.nCblk + a.nSblk;
     if (blocks > INT_MAX) return fail(ULP_EINVAL, "unpack: grid of %lld blocks", blocks);
+    return ULP_OK;
+}
+
+}  // namespace ulp
+
+using namespace ulp;
+
+extern "C" int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int D, int world_size,
+                                   int aligned, int scale_sequence, int q_group, int8_t *q8,
+                                   int8_t *k8, uint8_t *v8, float *q_scale, float *k_scale,
+                                   int num_dests, int enable_pdl, ulp_stream_t stream)
+{
+    if (enable_pdl < -1 || enable_pdl > 2) return fail(ULP_EINVAL, "unpack: enable_pdl must be -1, 0, 1 or 2");
+    UnpackArgs a;
+    long long blocks = 0;
+    if (int s = unpack_setup(a, blocks, recv, B, L, h, D, world_size, aligned, scale_sequence, q_group, q8, k8,
+                             v8, q_scale, k_scale, num_dests))
+        return s;
     const cudaStream_t st = (cudaStream_t)stream;
     const bool pdl = pdl_enabled(enable_pdl);
     if (D == 128) launch_kernel(unpack_kernel<128>, dim3((unsigned)blocks), dim3(kUnpackThreads), st, pdl, a);

@@ -32,7 +32,8 @@ class UlyssesLowpPath:
                  used_sequence: Optional[int] = None, scale_sequence: Optional[int] = None,
                  aligned: Optional[bool] = None, q_group: int = ulp.GQ, fused: bool = True,
                  fold_exchange: bool = True, fold_derive: Optional[bool] = None,
-                 pdl: Optional[bool] = None, pdl_unpack: Optional[bool] = None, device="cuda"):
+                 pdl: Optional[bool] = None, pdl_unpack: Optional[bool] = None,
+                 single_launch: Optional[bool] = None, device="cuda"):
         P = world_size
         self.B, self.L, self.H, self.D, self.P = B, L, H, D, P
         self.h = H // P
@@ -58,6 +59,20 @@ class UlyssesLowpPath:
         # CTAs would sit on SMs through pack's last wave)
         self.pdl_pack = 2 if pdl is None or pdl else 0
         self.pdl = launch_bound if pdl_unpack is None else bool(pdl_unpack)
+        # single_launch: the whole step as one cooperative launch
+        # (ulp.group_step: boundary min/max, pack with the derive and the
+        # exchange folded in, unpack).  Off unless asked for (None = off):
+        # chained by programmatic launch, the separate launches take less GPU
+        # time (each grid barrier costs about 2 us, and the fused kernel runs
+        # one CTA per SM); the single launch wins only where the host's
+        # launch rate bounds the step.  It needs the fused amax and the
+        # folded exchange.
+        can_single = fused and fold_exchange and fold_derive is not False
+        if single_launch and not can_single:
+            raise ValueError("single_launch needs fused=True, fold_exchange=True and fold_derive not False")
+        self.single_launch = bool(single_launch)
+        if self.single_launch:
+            self.fold_derive = True
         self.device = torch.device(device)
         self.chunk_bytes = ulp.chunk_bytes(B, L, self.h, D, q_group)
         f32 = dict(dtype=torch.float32, device=self.device)
@@ -69,9 +84,16 @@ class UlyssesLowpPath:
         self.send = None if fold_exchange else torch.empty((P, P, self.chunk_bytes), **u8)
         self.out = ulp.unpack_outputs(B, L, self.h, D, P, scale_sequence, self.device, num_dests=P,
                                       q_group=q_group)
+        # the single launch's grid barrier (zero before the first step; each
+        # step leaves it ready for the next) and its status word
+        i32 = dict(dtype=torch.int32, device=self.device)
+        self.barrier = torch.zeros(2, **i32) if self.single_launch else None
+        self.status = torch.zeros(1, **i32) if self.single_launch else None
 
     @property
     def launches_per_step(self) -> int:
+        if self.single_launch:
+            return 1
         return 3 + (0 if self.fold_derive else 1) + (0 if self.fused else 1) + (0 if self.fold_exchange else 1)
 
     def run(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, k_mean: torch.Tensor,
@@ -81,8 +103,21 @@ class UlyssesLowpPath:
         (q8, k8, v8, q_scale, k_scale), each with a leading P axis, in
         ``out`` (a tuple from ``new_outputs()``) or ``self.out``.
         ``on_pack`` (optional) is a pair of callables run right before and
-        after the pack launch (used to time it)."""
+        after the pack launch (used to time it); with the single launch, around
+        that launch."""
         P, L = self.P, self.L
+        if self.single_launch:
+            if on_pack is not None:
+                on_pack[0]()
+            res = ulp.group_step(q, k, v, k_mean, v_scale, world_size=P, minmax=self.minmax,
+                                 q_partial=self.q_partial, k_amax=self.k_amax, recv=self.recv,
+                                 out=self.out if out is None else out, barrier=self.barrier,
+                                 used_sequence=self.used_sequence, q_group=self.q_group,
+                                 aligned=self.aligned, scale_sequence=self.scale_sequence,
+                                 status=self.status)
+            if on_pack is not None:
+                on_pack[1]()
+            return res
         if not self.fused:
             ulp.k_grouped_amax(k, k_mean, rank=None, world_size=P,
                                used_sequence=self.used_sequence, out=self.k_amax)
@@ -107,6 +142,18 @@ class UlyssesLowpPath:
                                    aligned=self.aligned, scale_sequence=self.scale_sequence,
                                    q_group=self.q_group, out=self.out if out is None else out,
                                    enable_pdl=self.pdl)
+
+    def check_status(self):
+        """Raise if a single-launch step gave up at a grid barrier (reads the
+        status word, so it synchronises).  Zeroes the barrier and the status
+        first, so the next step starts clean."""
+        if self.status is None:
+            return
+        st = int(self.status.item())
+        if st != 0:
+            self.barrier.zero_()
+            self.status.zero_()
+            raise RuntimeError(f"group_step: a grid barrier timed out (status {st}); outputs undefined")
 
     def new_outputs(self):
         """A fresh set of device output tensors shaped like ``self.out``."""

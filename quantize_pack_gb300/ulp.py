@@ -74,12 +74,14 @@ def lib() -> ctypes.CDLL:
         L.ulp_sage_attention.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                          ctypes.c_float, _P, _SZ, _P, _I, _I, _P, _P]
         L.ulp_sage_attention_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]
+        L.ulp_group_step.argtypes = [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                                     _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
         for name in ("ulp_slots", "ulp_scale_widths", "ulp_chunk_bytes", "ulp_chunk_offsets",
                      "ulp_k_mean_workspace_bytes", "ulp_k_mean_global", "ulp_k_mean_global_noalloc",
                      "ulp_k_mean_global_grouped",
                      "ulp_k_grouped_amax", "ulp_boundary_minmax", "ulp_derive_k_boundary_amax",
                      "ulp_check_padding",
-                     "ulp_pack", "ulp_alltoall_emulate", "ulp_unpack_for_sage",
+                     "ulp_pack", "ulp_alltoall_emulate", "ulp_unpack_for_sage", "ulp_group_step",
                      "ulp_sage_attention", "ulp_sage_attention_workspace_bytes"):
             getattr(L, name).restype = _I
         _lib = L
@@ -375,6 +377,34 @@ def unpack_for_sage(recv_u8: torch.Tensor, *, batch_size: int, local_sequence: i
 # ------------------------------------------------------------- the consumer
 
 _OUT_CODES = {torch.float32: ULP_F32, torch.bfloat16: ULP_BF16, torch.float16: ULP_FP16}
+
+
+def group_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, k_mean_global: torch.Tensor,
+               v_scale: torch.Tensor, *, world_size: int, minmax: torch.Tensor,
+               q_partial: torch.Tensor, k_amax: torch.Tensor, recv: torch.Tensor,
+               out: Sequence[torch.Tensor], barrier: torch.Tensor,
+               used_sequence: Optional[int] = None, q_group: int = GQ,
+               aligned: Optional[bool] = None, scale_sequence: Optional[int] = None,
+               status: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, ...]:
+    """One step of the whole emulated group in one cooperative launch:
+    ``boundary_minmax`` (all ranks), ``pack`` with ``gathered_minmax``, fused,
+    dest-major into ``recv``, then ``unpack_for_sage`` of every destination
+    into ``out`` (five tensors with a leading P axis, see ``unpack_outputs``).
+    q, k, v: stacked shards [P, B, L, H, D].  ``barrier``: int32 device tensor
+    of two elements, zero before the first call (the kernel leaves it ready
+    for the next one; zero it again after a non-zero ``status``)."""
+    P = world_size
+    _, B, L, H, D = q.shape
+    if barrier.numel() < 2 or barrier.dtype not in (torch.int32, torch.uint32):
+        raise ValueError("barrier must be a 32-bit tensor of at least two elements")
+    q8, k8, v8, qs, ks = out
+    st = 0 if status is None else _ptr(status)
+    _check(lib().ulp_group_step(_ptr(q), _ptr(k), _ptr(v), _ptr(k_mean_global), _dtype_code(q),
+                                _ptr(v_scale), B, L, H, D, P, _opt(used_sequence), q_group,
+                                _tri(aligned), _opt(scale_sequence), _ptr(minmax), _ptr(q_partial),
+                                _ptr(k_amax), _ptr(recv), _ptr(q8), _ptr(k8), _ptr(v8), _ptr(qs),
+                                _ptr(ks), _ptr(barrier), st, _stream(q.device)))
+    return tuple(out)
 
 
 def sage_attention(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale: torch.Tensor,

@@ -92,11 +92,14 @@ def test_codec_adversarial(dtype, D, seed):
     wl = inp.wl
     res = hp.run_oracle(inp)
     q, k, v, km, vs = gh.to_device(inp)
-    path = UlyssesLowpPath(B=wl.B, L=wl.L, H=wl.H, D=wl.D, world_size=wl.P,
-                           dtype=gh.torch_dtype(wl.dtype))
-    outs = path.run(q, k, v, km, vs)
-    torch.cuda.synchronize()
-    gh.assert_bits_equal(path.recv, res["recv"], "chunks")
-    for i, name in enumerate(["q8", "k8", "v8", "q_scale", "k_scale"]):
-        want = np.stack([res["out"][p][i] for p in range(wl.P)])
-        gh.assert_bits_equal(outs[i], want, name)
+    # the pack kernel of the three-launch step, and the same body inside the
+    # single cooperative launch
+    for single in (False, True):
+        path = UlyssesLowpPath(B=wl.B, L=wl.L, H=wl.H, D=wl.D, world_size=wl.P,
+                               dtype=gh.torch_dtype(wl.dtype), single_launch=single)
+        outs = path.run(q, k, v, km, vs)
+        torch.cuda.synchronize()
+        gh.assert_bits_equal(path.recv, res["recv"], f"chunks (single launch {single})")
+        for i, name in enumerate(["q8", "k8", "v8", "q_scale", "k_scale"]):
+            want = np.stack([res["out"][p][i] for p in range(wl.P)])
+            gh.assert_bits_equal(outs[i], want, f"{name} (single launch {single})")

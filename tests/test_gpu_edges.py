@@ -123,7 +123,8 @@ def test_programmatic_launch_on_and_off(pdl):
     inp, res, (q, k, v, km, vs) = _setup(wl)
     path = UlyssesLowpPath(B=wl.B, L=wl.L, H=wl.H, D=wl.D, world_size=wl.P,
                            dtype=gh.torch_dtype(wl.dtype), used_sequence=wl.used_sequence,
-                           scale_sequence=wl.scale_sequence, pdl=pdl)
+                           scale_sequence=wl.scale_sequence, pdl=pdl, pdl_unpack=pdl,
+                           single_launch=False)
     for _ in range(3):
         outs = path.run(q, k, v, km, vs)
     torch.cuda.synchronize()
@@ -131,11 +132,13 @@ def test_programmatic_launch_on_and_off(pdl):
         gh.assert_bits_equal(outs[i], np.stack([res["out"][p][i] for p in range(wl.P)]), name)
 
 
-def test_cuda_graph_replay_with_new_inputs():
+@pytest.mark.parametrize("single", [False, True], ids=["three_launches", "single_launch"])
+def test_cuda_graph_replay_with_new_inputs(single):
     wl = hp.SIX
     path = UlyssesLowpPath(B=wl.B, L=wl.L, H=wl.H, D=wl.D, world_size=wl.P,
                            dtype=gh.torch_dtype(wl.dtype), used_sequence=wl.used_sequence,
-                           scale_sequence=wl.scale_sequence)
+                           scale_sequence=wl.scale_sequence, single_launch=single)
+    assert path.launches_per_step == (1 if single else 3)
     inp0 = synth.make_inputs(wl)
     q, k, v, km, vs = gh.to_device(inp0)
     graph = path.capture(q, k, v, km, vs)
@@ -148,6 +151,7 @@ def test_cuda_graph_replay_with_new_inputs():
         torch.cuda.synchronize()
         for i, name in enumerate(["q8", "k8", "v8", "q_scale", "k_scale"]):
             gh.assert_bits_equal(path.out[i], np.stack([res["out"][p][i] for p in range(wl.P)]), name)
+        path.check_status()
 
 
 def test_host_pipeline_runs_consecutive_steps():

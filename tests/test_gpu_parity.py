@@ -126,22 +126,25 @@ def test_alltoall_and_unpack(wl):
             gh.assert_bits_equal(one[i], res["out"][p][i], f"{name} dest {p}")
 
 
-@pytest.mark.parametrize("mode", ["fused_folded", "unfused_copy", "fused_separate_derive"])
+@pytest.mark.parametrize("mode", ["fused_folded", "unfused_copy", "fused_separate_derive", "single_launch"])
 @pytest.mark.parametrize("wl", GPU_WORKLOADS, ids=lambda w: w.name)
 def test_whole_path(wl, mode):
     """The step through UlyssesLowpPath: fused pack with the exchange and the
     derive folded in (three launches); the unfused pack, the derive folded,
     with the all-to-all as its own copy; the fused pack after a separate
-    derive launch."""
+    derive launch; the whole step as one cooperative launch (ulp.group_step),
+    whose grid barrier must come back to a zero count after every step."""
     inp, res, (q, k, v, km, vs) = _setup(wl)
     path = UlyssesLowpPath(B=wl.B, L=wl.L, H=wl.H, D=wl.D, world_size=wl.P,
                            dtype=gh.torch_dtype(wl.dtype), used_sequence=wl.used_sequence,
                            scale_sequence=wl.scale_sequence, aligned=wl.aligned,
                            q_group=wl.q_group, fused=(mode != "unfused_copy"),
                            fold_exchange=(mode != "unfused_copy"),
-                           fold_derive=(mode != "fused_separate_derive"))
-    assert path.launches_per_step == {"fused_folded": 3, "unfused_copy": 5, "fused_separate_derive": 4}[mode]
-    for _ in range(2):                      # a second step on the same buffers
+                           fold_derive=(mode != "fused_separate_derive"),
+                           single_launch=(mode == "single_launch"))
+    assert path.launches_per_step == {"fused_folded": 3, "unfused_copy": 5, "fused_separate_derive": 4,
+                                      "single_launch": 1}[mode]
+    for step in range(2):                   # a second step on the same buffers
         outs = path.run(q, k, v, km, vs)
         torch.cuda.synchronize()
         for i, name in enumerate(["q8", "k8", "v8", "q_scale", "k_scale"]):
@@ -149,3 +152,10 @@ def test_whole_path(wl, mode):
             gh.assert_bits_equal(outs[i], want, name)
         gh.assert_bits_equal(path.recv, res["recv"], "recv")
         gh.assert_bits_equal(path.k_amax, res["amax"], "k_amax")
+        if mode == "single_launch":
+            path.check_status()
+            # two barriers a step: the count is back at zero, the generation
+            # advanced by two
+            assert path.barrier.tolist() == [0, 2 * (step + 1)]
+            gh.assert_bits_equal(path.minmax, res["minmax"], "minmax")
+            gh.assert_bits_equal(path.q_partial, res["qb"], "q_partial")
