@@ -17,8 +17,9 @@
  *                               Returns: the V scale stays with the caller)
  *   ulp_alltoall_emulate        the all-to-all of the chunks, as a device-local copy
  *   ulp_unpack_for_sage         page "...unpack_for_sage"
- *   ulp_group_step              boundary min/max + pack (derive and exchange folded) +
- *                               unpack of a whole emulated group in one launch
+ *   ulp_group_step              boundary min/max + pack (exchange folded) + unpack of a
+ *                               whole emulated group from one call (its launches, or one
+ *                               cooperative launch)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -299,36 +300,48 @@ int ulp_unpack_for_sage(const uint8_t *recv, int B, int L, int h, int D, int wor
                         uint8_t *v8, float *q_scale, float *k_scale, int num_dests,
                         int enable_pdl, ulp_stream_t stream);
 
-/* One step of an emulated Ulysses group (every rank, every destination) in a
- * single cooperative launch: ulp_boundary_minmax (ULP_ALL_RANKS), then
- * ulp_pack with gathered_minmax given (the boundary derive of page
- * "derive_k_boundary_amax" folded in), fused = 1 and ULP_SEND_DEST_MAJOR
- * into recv (the all-to-all folded into the stores; page "unpack_for_sage",
- * recv_u8), then ulp_unpack_for_sage of all P destinations
- * (num_dests = world_size).  Every output equals, bit for bit, that of
- * those three calls with the same arguments: minmax [P, B, H, 2, 2, D] and
- * q_partial [P, B, H, 2] as written by ulp_boundary_minmax, k_amax
+/* Modes of ulp_group_step (bits). */
+enum {
+    ULP_STEP_COOPERATIVE = 1,       /* one cooperative launch (no other bit) */
+    ULP_STEP_DERIVE_SEPARATE = 2,   /* separate launches: the boundary derive as its own launch */
+    ULP_STEP_UNPACK_PDL = 4         /* separate launches: unpack as a programmatic dependent launch */
+};
+
+/* One step of an emulated Ulysses group (every rank, every destination) from
+ * one call: ulp_boundary_minmax (ULP_ALL_RANKS), then ulp_pack with fused = 1
+ * and ULP_SEND_DEST_MAJOR into recv (the all-to-all folded into the stores;
+ * page "unpack_for_sage", recv_u8), with the boundary derive of page
+ * "derive_k_boundary_amax" folded into pack (gathered_minmax given) or, with
+ * ULP_STEP_DERIVE_SEPARATE, as ulp_derive_k_boundary_amax before it; then
+ * ulp_unpack_for_sage of all P destinations (num_dests = world_size).  Every
+ * output equals, bit for bit, that of those calls: minmax [P, B, H, 2, 2, D]
+ * and q_partial [P, B, H, 2] as written by ulp_boundary_minmax, k_amax
  * [P, B, H, slots(L,64)] as by ulp_pack, recv [P_dst, P_src, chunk_bytes],
- * and the unpacked q8, k8, v8, q_scale, k_scale with a leading P axis.  It
- * takes one launch instead of three: it helps where the host's launch rate
- * bounds the step (small steps called eagerly).  In GPU time the three
- * launches chained by programmatic launch are faster: each grid barrier
- * costs about 2 us, and the fused kernel runs one CTA per SM.
- *   The phases are separated by grid-wide barriers in `barrier`: two 32-bit
- *   words of device memory (4-byte aligned) that must be zero before the
- *   first call and that every completed call leaves zero-count again.  Calls
- *   that may run concurrently (other streams) need their own pair.  Each
- *   barrier wait is bounded (1 s); on a timeout the kernel writes 2 to
- *   *status (a device int, or NULL) and returns early with outputs
- *   undefined, and the pair must be zeroed again before the next call.  A
- *   cooperative launch needs every CTA resident, so the grid is capped by the
- *   occupancy of the device; a launch that still cannot be made gives
+ * and the unpacked q8, k8, v8, q_scale, k_scale with a leading P axis.  All
+ * arguments are checked before the first launch.
+ *   mode without ULP_STEP_COOPERATIVE: the separate launches (three, or four
+ *   with the derive), pack reading its inputs before its predecessor
+ *   completes (enable_pdl = 2), unpack programmatic only with
+ *   ULP_STEP_UNPACK_PDL.  One call instead of three or four, the same GPU
+ *   work; barrier and status are ignored (may be NULL).
+ *   mode = ULP_STEP_COOPERATIVE: one cooperative kernel runs the three phases
+ *   (the derive folded) separated by grid-wide barriers.  It helps only where
+ *   the host's launch rate bounds the step; in GPU time the chained launches
+ *   are faster (each grid barrier costs about 2 us, and the fused kernel runs
+ *   one CTA per SM).  `barrier`: two 32-bit words of device memory (4-byte
+ *   aligned) that must be zero before the first call; every completed call
+ *   leaves the count zero again.  Calls that may run concurrently (other
+ *   streams) need their own pair.  Each barrier wait is bounded (1 s); on a
+ *   timeout the kernel writes 2 to *status (a device int, or NULL) and returns
+ *   early with outputs undefined, and the pair must be zeroed again before
+ *   the next call.  The grid is capped by the device's occupancy so that
+ *   every CTA is resident; a launch that still cannot be made gives
  *   ULP_ECUDA. */
 int ulp_group_step(const void *q, const void *k, const void *v, const void *k_mean, int dtype,
                    const float *v_scale, int B, int L, int H, int D, int world_size, int used_sequence,
                    int q_group, int aligned, int scale_sequence, float *minmax, float *q_partial,
                    float *k_amax, uint8_t *recv, int8_t *q8, int8_t *k8, uint8_t *v8, float *q_scale,
-                   float *k_scale, unsigned *barrier, int *status, ulp_stream_t stream);
+                   float *k_scale, int mode, unsigned *barrier, int *status, ulp_stream_t stream);
 
 /* Attention over the unpacked tensors of one destination -- the consumer the
  * page "unpack_for_sage" hands its outputs to (INT8 Q/K, FP8 E4M3 V, FP32

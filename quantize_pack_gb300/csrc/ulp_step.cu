@@ -1,5 +1,6 @@
-// One step of the emulated Ulysses group in a single cooperative launch, for
-// steps too small to hide three launches (a few MB to ~L2-sized inputs):
+// One step of the emulated Ulysses group from one call: either the separate
+// launches the path's entry points make (chained by programmatic launch), or
+// a single cooperative launch that runs:
 //  1. the raw-K boundary min/max and the Q boundary partials of every rank
 //     (the gathered buffers of page "derive_k_boundary_amax");
 //  2. the sender pack of every rank, with the boundary derive (page
@@ -169,13 +170,20 @@ extern "C" int ulp_group_step(const void *q, const void *k, const void *v, const
                               const float *v_scale, int B, int L, int H, int D, int world_size,
                               int used_sequence, int q_group, int aligned, int scale_sequence, float *minmax,
                               float *q_partial, float *k_amax, uint8_t *recv, int8_t *q8, int8_t *k8,
-                              uint8_t *v8, float *q_scale, float *k_scale, unsigned *barrier, int *status,
-                              ulp_stream_t stream)
+                              uint8_t *v8, float *q_scale, float *k_scale, int mode, unsigned *barrier,
+                              int *status, ulp_stream_t stream)
 {
+    const bool coop = (mode & ULP_STEP_COOPERATIVE) != 0;
+    const bool derive_separate = (mode & ULP_STEP_DERIVE_SEPARATE) != 0;
+    if (mode < 0 || mode > (ULP_STEP_COOPERATIVE | ULP_STEP_DERIVE_SEPARATE | ULP_STEP_UNPACK_PDL))
+        return fail(ULP_EINVAL, "group_step: unknown mode bits (%d)", mode);
+    if (coop && mode != ULP_STEP_COOPERATIVE)
+        return fail(ULP_EINVAL, "group_step: the cooperative launch takes no other mode bit (%d)", mode);
     StepArgs s{};
     dim3 grid;
     // pack's checks cover the inputs, the sizes, k_amax, the partials, the
-    // min/max buffer and recv; unpack's cover its outputs
+    // min/max buffer and recv; unpack's cover its outputs.  Everything is
+    // checked before the first launch.
     if (int r = pack_setup(s.pk, grid, q, k, v, k_mean, dtype, k_amax, q_partial, minmax, v_scale, B, L, H, D,
                            ULP_ALL_RANKS, world_size, used_sequence, q_group, 1, recv, ULP_SEND_DEST_MAJOR))
         return r;
@@ -183,6 +191,26 @@ extern "C" int ulp_group_step(const void *q, const void *k, const void *v, const
     if (int r = unpack_setup(s.up, s.n_up, recv, B, L, H / world_size, D, world_size, aligned, scale_sequence,
                              q_group, q8, k8, v8, q_scale, k_scale, world_size))
         return r;
+    if (!coop) {
+        // the separate launches: boundary min/max, [derive,] pack (reading
+        // its inputs before its predecessor completes: neither writes them),
+        // unpack -- each entry point as its own call would make them
+        const cudaStream_t st = (cudaStream_t)stream;
+        if (int r = ulp_boundary_minmax(k, q, dtype, B, L, H, D, ULP_ALL_RANKS, world_size, used_sequence, q_group,
+                                        minmax, q_partial, st))
+            return r;
+        if (derive_separate) {
+            if (int r = ulp_derive_k_boundary_amax(k_amax, minmax, k_mean, dtype, B, H, D, ULP_ALL_RANKS, L,
+                                                   world_size, st))
+                return r;
+        }
+        if (int r = ulp_pack(q, k, v, k_mean, dtype, k_amax, q_partial, derive_separate ? nullptr : minmax, v_scale,
+                             B, L, H, D, ULP_ALL_RANKS, world_size, used_sequence, q_group, 1, recv,
+                             ULP_SEND_DEST_MAJOR, 2, st))
+            return r;
+        return ulp_unpack_for_sage(recv, B, L, H / world_size, D, world_size, aligned, scale_sequence, q_group, q8,
+                                   k8, v8, q_scale, k_scale, world_size, (mode & ULP_STEP_UNPACK_PDL) ? 1 : 0, st);
+    }
     if (!barrier || !aligned4(barrier)) return fail(ULP_EALIGN, "group_step: barrier must be a 4-byte aligned pair");
     if (status && !aligned4(status)) return fail(ULP_EALIGN, "group_step: status must be 4-byte aligned");
     s.mm = MinmaxArgs{(const uint16_t *)k, (const uint16_t *)q, minmax, q_partial, B, L, H, world_size,

@@ -106,18 +106,23 @@ class UlyssesLowpPath:
         after the pack launch (used to time it); with the single launch, around
         that launch."""
         P, L = self.P, self.L
+        step = dict(world_size=P, minmax=self.minmax, q_partial=self.q_partial, k_amax=self.k_amax,
+                    recv=self.recv, out=self.out if out is None else out,
+                    used_sequence=self.used_sequence, q_group=self.q_group, aligned=self.aligned,
+                    scale_sequence=self.scale_sequence)
         if self.single_launch:
             if on_pack is not None:
                 on_pack[0]()
-            res = ulp.group_step(q, k, v, k_mean, v_scale, world_size=P, minmax=self.minmax,
-                                 q_partial=self.q_partial, k_amax=self.k_amax, recv=self.recv,
-                                 out=self.out if out is None else out, barrier=self.barrier,
-                                 used_sequence=self.used_sequence, q_group=self.q_group,
-                                 aligned=self.aligned, scale_sequence=self.scale_sequence,
-                                 status=self.status)
+            res = ulp.group_step(q, k, v, k_mean, v_scale, mode=ulp.STEP_COOPERATIVE, barrier=self.barrier,
+                                 status=self.status, **step)
             if on_pack is not None:
                 on_pack[1]()
             return res
+        if self.fused and self.fold_exchange and self.pdl_pack == 2 and on_pack is None:
+            # the same launches from one call into the library (less host
+            # time per step where the host's launch rate bounds it)
+            mode = (0 if self.fold_derive else ulp.STEP_DERIVE_SEPARATE) | (ulp.STEP_UNPACK_PDL if self.pdl else 0)
+            return ulp.group_step(q, k, v, k_mean, v_scale, mode=mode, **step)
         if not self.fused:
             ulp.k_grouped_amax(k, k_mean, rank=None, world_size=P,
                                used_sequence=self.used_sequence, out=self.k_amax)

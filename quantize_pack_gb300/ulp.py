@@ -26,6 +26,9 @@ ULP_BF16, ULP_FP16, ULP_F32 = 0, 1, 2
 ULP_ALL_RANKS = -1
 SEND_SOURCE_MAJOR, SEND_DEST_MAJOR = 0, 1
 PV_F16, PV_E4M3 = 0, 1   # precision of the attention's PV product
+# group_step mode bits: one cooperative launch; else separate launches, with the
+# derive as its own launch and/or unpack launched programmatically
+STEP_COOPERATIVE, STEP_DERIVE_SEPARATE, STEP_UNPACK_PDL = 1, 2, 4
 GK, GQ = 64, 128   # K group rows; default Q group rows (q_group=64 selects the other width)
 
 _STATUS = {-1: "EINVAL", -2: "EDTYPE", -3: "EALIGN", -4: "ECUDA"}
@@ -75,7 +78,7 @@ def lib() -> ctypes.CDLL:
                                          ctypes.c_float, _P, _SZ, _P, _I, _I, _P, _P]
         L.ulp_sage_attention_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]
         L.ulp_group_step.argtypes = [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
-                                     _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+                                     _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P]
         for name in ("ulp_slots", "ulp_scale_widths", "ulp_chunk_bytes", "ulp_chunk_offsets",
                      "ulp_k_mean_workspace_bytes", "ulp_k_mean_global", "ulp_k_mean_global_noalloc",
                      "ulp_k_mean_global_grouped",
@@ -382,28 +385,33 @@ _OUT_CODES = {torch.float32: ULP_F32, torch.bfloat16: ULP_BF16, torch.float16: U
 def group_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, k_mean_global: torch.Tensor,
                v_scale: torch.Tensor, *, world_size: int, minmax: torch.Tensor,
                q_partial: torch.Tensor, k_amax: torch.Tensor, recv: torch.Tensor,
-               out: Sequence[torch.Tensor], barrier: torch.Tensor,
+               out: Sequence[torch.Tensor], mode: int = 0, barrier: Optional[torch.Tensor] = None,
                used_sequence: Optional[int] = None, q_group: int = GQ,
                aligned: Optional[bool] = None, scale_sequence: Optional[int] = None,
                status: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, ...]:
-    """One step of the whole emulated group in one cooperative launch:
-    ``boundary_minmax`` (all ranks), ``pack`` with ``gathered_minmax``, fused,
-    dest-major into ``recv``, then ``unpack_for_sage`` of every destination
-    into ``out`` (five tensors with a leading P axis, see ``unpack_outputs``).
-    q, k, v: stacked shards [P, B, L, H, D].  ``barrier``: int32 device tensor
-    of two elements, zero before the first call (the kernel leaves it ready
-    for the next one; zero it again after a non-zero ``status``)."""
+    """One step of the whole emulated group from one call: ``boundary_minmax``
+    (all ranks), ``pack`` fused, dest-major into ``recv`` (the derive folded
+    in, or before it with STEP_DERIVE_SEPARATE), then ``unpack_for_sage`` of
+    every destination into ``out`` (five tensors with a leading P axis, see
+    ``unpack_outputs``).  q, k, v: stacked shards [P, B, L, H, D].
+    ``mode``: 0 or STEP_DERIVE_SEPARATE | STEP_UNPACK_PDL bits for the
+    separate launches; STEP_COOPERATIVE for one cooperative launch, which
+    needs ``barrier`` (a 32-bit device tensor of two elements, zero before the
+    first call; the kernel leaves it ready for the next one; zero it again
+    after a non-zero ``status``)."""
     P = world_size
     _, B, L, H, D = q.shape
-    if barrier.numel() < 2 or barrier.dtype not in (torch.int32, torch.uint32):
-        raise ValueError("barrier must be a 32-bit tensor of at least two elements")
+    coop = bool(mode & STEP_COOPERATIVE)
+    if coop and (barrier is None or barrier.numel() < 2 or barrier.dtype not in (torch.int32, torch.uint32)):
+        raise ValueError("the cooperative launch needs barrier: a 32-bit tensor of at least two elements")
     q8, k8, v8, qs, ks = out
     st = 0 if status is None else _ptr(status)
+    bar = _ptr(barrier) if coop else None
     _check(lib().ulp_group_step(_ptr(q), _ptr(k), _ptr(v), _ptr(k_mean_global), _dtype_code(q),
                                 _ptr(v_scale), B, L, H, D, P, _opt(used_sequence), q_group,
                                 _tri(aligned), _opt(scale_sequence), _ptr(minmax), _ptr(q_partial),
                                 _ptr(k_amax), _ptr(recv), _ptr(q8), _ptr(k8), _ptr(v8), _ptr(qs),
-                                _ptr(ks), _ptr(barrier), st, _stream(q.device)))
+                                _ptr(ks), int(mode), bar, st, _stream(q.device)))
     return tuple(out)
 
 

@@ -139,14 +139,14 @@ def test_group_step_rejects(lib):
     barrier pair, the status word)."""
     ok = dict(q=FAKE, k=FAKE, v=FAKE, km=FAKE, dt=0, vs=FAKE, B=1, L=96, H=8, D=64, P=2, used=-1, gq=128,
               aligned=-1, sseq=-1, mm=FAKE, qp=FAKE, amax=FAKE, recv=FAKE, q8=FAKE, k8=FAKE, v8=FAKE, qs=FAKE,
-              ks=FAKE, bar=FAKE, st=FAKE)
+              ks=FAKE, mode=1, bar=FAKE, st=FAKE)
 
     def call(**kw):
         a = dict(ok, **kw)
         return lib.ulp_group_step(a["q"], a["k"], a["v"], a["km"], a["dt"], a["vs"], a["B"], a["L"], a["H"],
                                   a["D"], a["P"], a["used"], a["gq"], a["aligned"], a["sseq"], a["mm"],
                                   a["qp"], a["amax"], a["recv"], a["q8"], a["k8"], a["v8"], a["qs"], a["ks"],
-                                  a["bar"], a["st"], None)
+                                  a["mode"], a["bar"], a["st"], None)
     assert call(bar=FAKE + 2) == -3 and b"barrier" in lib.ulp_last_error()
     assert call(bar=None) == -3
     assert call(st=FAKE + 1) == -3
@@ -157,3 +157,9 @@ def test_group_step_rejects(lib):
     assert call(v8=FAKE + 1) == -3                                         # unpack's
     assert call(P=5) == -1 and call(D=32) == -1 and call(dt=7) == -2
     assert call(used=193) == -1 and call(sseq=0) == -1
+    # modes: unknown bits, the cooperative launch with another bit; the
+    # separate launches validate everything before the first one
+    assert call(mode=8) == -1 and call(mode=-1) == -1
+    assert call(mode=3) == -1 and call(mode=5) == -1
+    assert call(mode=0, bar=None, aligned=1) == -1 and b"aligned" in lib.ulp_last_error()
+    assert call(mode=6, bar=None, mm=None) == -1 and b"minmax" in lib.ulp_last_error()
