@@ -176,3 +176,28 @@ def test_host_pipeline_runs_consecutive_steps():
     for step, (got, exp) in enumerate(zip(host_out, want)):
         for i, name in enumerate(["q8", "k8", "v8", "q_scale", "k_scale"]):
             gh.assert_bits_equal(got[i], exp[i], f"step {step} {name}")
+
+
+def test_group_step_barrier_timeout_reports_status():
+    """The cooperative step's grid barrier gives up after its bound: with the
+    arrival count preset far from any CTA's completing arrival, every CTA
+    waits its 1 s, the kernel writes status 2 and returns (nothing hangs);
+    check_status() raises, zeroes the barrier pair, and the next step is
+    bit-exact again."""
+    wl = hp.TINY
+    inp, res, (q, k, v, km, vs) = _setup(wl)
+    path = UlyssesLowpPath(B=wl.B, L=wl.L, H=wl.H, D=wl.D, world_size=wl.P,
+                           dtype=gh.torch_dtype(wl.dtype), used_sequence=wl.used_sequence,
+                           scale_sequence=wl.scale_sequence, single_launch=True)
+    path.barrier[0] = 1 << 30                 # no arrival can make the count complete
+    path.run(q, k, v, km, vs)
+    torch.cuda.synchronize()
+    assert int(path.status.item()) == 2
+    with pytest.raises(RuntimeError, match="timed out"):
+        path.check_status()
+    assert path.barrier.tolist() == [0, 0] and int(path.status.item()) == 0
+    outs = path.run(q, k, v, km, vs)
+    torch.cuda.synchronize()
+    path.check_status()
+    for i, name in enumerate(["q8", "k8", "v8", "q_scale", "k_scale"]):
+        gh.assert_bits_equal(outs[i], np.stack([res["out"][p][i] for p in range(wl.P)]), name)
