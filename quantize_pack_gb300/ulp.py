@@ -399,11 +399,11 @@ def group_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, k_mean_global:
     needs ``barrier`` (a 32-bit device tensor of two elements, zero before the
     first call; the kernel leaves it ready for the next one; zero it again
     after a non-zero ``status``)."""
-    P = world_size
-    _, B, L, H, D = q.shape
     coop = bool(mode & STEP_COOPERATIVE)
     if coop and (barrier is None or barrier.numel() < 2 or barrier.dtype not in (torch.int32, torch.uint32)):
         raise ValueError("the cooperative launch needs barrier: a 32-bit tensor of at least two elements")
+    P = world_size
+    _, B, L, H, D = q.shape
     q8, k8, v8, qs, ks = out
     st = 0 if status is None else _ptr(status)
     bar = _ptr(barrier) if coop else None
